@@ -1,0 +1,356 @@
+#!/usr/bin/env python
+"""Benchmark of the fused linear cross-entropy forward+backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl flce|reference]
+
+One step = one call of flce_fwd_bwd over one batch of seeded synthetic input
+(all stages of the path: valid-row compaction, logits GEMM with the online
+log-sum-exp epilogue, dlogits, the grad_hidden and grad_weight GEMMs, the
+loss reduction).  Inputs are resident in HBM when the timed region starts;
+the weight (1 GB at the default workload) is larger than L2, so no flush is
+needed between steps.  Rank 0 prints one JSON line.
+
+With torchrun (N > 1) every rank runs an independent replica on its own
+batch (weak scaling): the path has no exchange step.
+
+``--impl reference`` times the fp64 CPU oracle instead (a deliberately slow
+program), each step a bounded sample of rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused linear-CE fwd+bwd tokens/s and % of GB300 dense BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(dev_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_time(p, rows):
+    """Run the fp64 oracle, as it stands, on the first `rows` valid tokens."""
+    import numpy as np
+    from oracle import flce_oracle
+    t = p["targets"]
+    sel = np.nonzero(t != -100)[0][:rows]
+    t0 = time.perf_counter()
+    flce_oracle(p["hidden"][sel], p["weight"], t[sel])
+    return time.perf_counter() - t0, int(sel.size)
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(p, target_s=12.0):
+    rows = 16
+    dt, n = oracle_sample_time(p, rows)
+    rows = int(max(16, min(4096, rows * target_s / max(dt, 1e-3))))
+    dt, n = oracle_sample_time(p, rows)
+    w = p["workload"]
+    return {"value": n / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, full fwd+bwd of the first {n} valid tokens of {w.name} "
+                      f"(H={w.H}, V={w.V}, full weight), {dt:.2f} s"}
+
+
+def run_reference(args):
+    import numpy as np  # noqa: F401
+    from linear_cross_entropy_ce_gb300 import workloads as wl
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.workload]
+    p = wl.make_inputs(w)
+    # size each step to about 3 s of CPU work
+    dt, n = oracle_sample_time(p, 8)
+    rows = int(max(8, min(2048, 8 * 3.0 / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_time(p, rows)
+    times = []
+    for _ in range(args.steps):
+        dt, n = oracle_sample_time(p, rows)
+        times.append(dt)
+    ms = 1000.0 * sum(times) / len(times)
+    value = n / (ms / 1000.0)
+    cores = cpu_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "sample_rows_per_step": n},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {n} valid tokens of {w.name} per step, full weight"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama3_8b_head")
+    ap.add_argument("--impl", default="flce", choices=["flce", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "flce":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from linear_cross_entropy_ce_gb300 import flce, workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flce.library()
+
+    base = wl.WORKLOADS[args.workload]
+    w = base.with_shape(seed=base.seed + 1000 * rank) if rank else base
+    p = wl.make_inputs(w)
+    N, H, V = w.N, w.H, w.V
+    h = torch.from_numpy(p["hidden"].view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(p["weight"].view(np.int16)).view(torch.bfloat16).to(dev)
+    t = torch.from_numpy(p["targets"]).to(dev)
+    nv = int((p["targets"] != -100).sum())
+    ws_bytes = flce.workspace_bytes(N, H, V)
+    plan = flce.plan(N, H, V, ws_bytes)
+    ws = flce.new_workspace(ws_bytes, dev)
+    out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+           "n_valid": torch.empty(1, dtype=torch.int32, device=dev),
+           "grad_hidden": torch.empty((N, H), dtype=torch.bfloat16, device=dev),
+           "grad_weight": torch.empty((V, H), dtype=torch.float32, device=dev), "row_loss": None}
+    stream = torch.cuda.current_stream()
+
+    def step():
+        flce.fwd_bwd(h, W, t, workspace=ws, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = flce.query_status(ws)
+    if st != flce.FLCE_OK:
+        raise RuntimeError(f"device status {flce.STATUS_NAMES[st]}")
+
+    clocks = ClockSampler(gpu_id_for(local))
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    flce.profile_begin()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    prof = flce.profile_end()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        m = torch.tensor([ms], device=dev)
+        dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        ms = float(m.item())
+
+    # end to end through the public API: pinned host inputs in, loss out, every step
+    e2e = None
+    if not args.no_e2e:
+        h_host = torch.from_numpy(p["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        t_host = torch.from_numpy(p["targets"]).pin_memory()
+        loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
+        h_dev, t_dev = torch.empty_like(h), torch.empty_like(t)
+
+        def e2e_step():
+            h_dev.copy_(h_host, non_blocking=True)
+            t_dev.copy_(t_host, non_blocking=True)
+            flce.fwd_bwd(h_dev, W, t_dev, workspace=ws, out=out, stream=stream)
+            loss_host[0:1].copy_(out["loss"], non_blocking=True)
+            loss_host[1:2].copy_(out["n_valid"].view(torch.float32), non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a0.elapsed_time(a1) / args.steps
+        if world > 1:
+            m = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(m, op=dist.ReduceOp.MAX)
+            e2e_ms = float(m.item())
+        e2e = {"value": world * N / (e2e_ms / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": N * H * 2 + N * 4, "d2h_bytes_per_step": 8,
+               "ms_per_step": e2e_ms, "note": "hidden and targets copied from pinned host memory each step, "
+                                             "loss and n_valid read back; the weight stays resident"}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    pk, src = peaks()
+    flops_alg = 6.0 * nv * H * V
+    gemm_ms = sum(prof["gemm_ms"].values())
+    gemm_n = sum(prof["gemm_launches"].values())
+    achieved = flops_alg * args.steps / (gemm_ms / 1000.0) / 1e12 if gemm_ms > 0 else None
+    peak_s = float(pk["bf16_tflops_sustained"])
+    peak_b = float(pk["bf16_tflops"])
+    step_tflops = flops_alg / (ms / 1000.0) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            if tj.get("workload") == w.name and tj.get("kernel_build") == flce.version():
+                traffic = tj.get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak_s, "unit": "TFLOP/s",
+            "frac": (achieved / peak_s) if achieved else None, "traffic": traffic,
+            "kernel": "flce_gemm_kernel (tcgen05, all three GEMM modes)",
+            "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step)",
+            "flops_per_launch": flops_alg / max(1, gemm_n / args.steps),
+            "avg_launch_ms": gemm_ms / max(1, gemm_n),
+            "per_mode_ms_per_step": {k: v / args.steps for k, v in prof["gemm_ms"].items()}}
+    line = {
+        "metric": METRIC, "value": world * N / (ms / 1000.0), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "N": N, "H": H, "V": V, "n_valid": nv, "chunk_rows": plan["chunk_rows"],
+                   "workspace_bytes": ws_bytes, "extra_mem_frac_of_NV2": ws_bytes / (N * V * 2),
+                   "l2": "inputs larger than L2 (weight alone exceeds 129 MB), no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_bf16_peak": {"value": 100.0 * step_tflops / peak_b, "tflops_alg": step_tflops,
+                          "basis": f"6*n_valid*H*V per step over step time, vs {src} bf16 burst peak {peak_b}",
+                          "vs_sustained": 100.0 * step_tflops / peak_s},
+        "roofline": roof,
+        "gpu_launches": prof["kernel_launches"],
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,179 @@
+/*
+ * flce.h - fused linear cross-entropy (LM head) on GB300 (sm_103a).
+ *
+ * The operation ("efficient-llm-anatomy" README, section "Fused cross-entropy
+ * computes backward during forward", and the "Per-component memory savings"
+ * table, row "Cross-entropy"): the LM-head matmul, softmax and negative
+ * log-likelihood are computed chunk by chunk over tokens, so the N x V logits
+ * are never materialised, and grad_input / grad_weight are produced in the
+ * same call as the loss.
+ *
+ * Notation:
+ *   X  = hidden      [N, H] bf16, row-major (row n is token n)
+ *   W  = weight      [V, H] bf16, row-major (PyTorch Linear layout: forward
+ *                    is X @ W^T; "Alisa's book of LLMs", "Neural net basics",
+ *                    linear-layer backprop paragraph)
+ *   t  = targets     [N] int32; t[n] == ignore_index marks an ignored token.
+ *                    Targets are NOT shifted inside the library: t[n] labels
+ *                    row n (the shift is the caller's business, as in the
+ *                    "implementing the loss" code of the same page).
+ *   z  = X W^T, lse_n = log sum_v exp(z_nv), loss_n = lse_n - z_{n,t_n}
+ *   loss = sum over valid n of loss_n / n_valid          (FLCE_REDUCE_MEAN)
+ *        = sum over valid n of loss_n                    (FLCE_REDUCE_SUM)
+ *   dz_nv = (softmax(z_n)_v - [v == t_n]) * s,  s = 1/n_valid (mean) or 1
+ *           ("gradient of softmax + CE loss" section; the 1/n from the
+ *           linearity of the mean, "Backpropagation" section)
+ *   grad_hidden = dz W    (bf16 [N, H]; rows of ignored tokens are +0.0)
+ *   grad_weight = dz^T X  (fp32 [V, H]; gradients accumulate in fp32, the
+ *                          mixed-precision convention of the same page)
+ *   When no token is valid (n_valid == 0) the loss and both gradients are 0.
+ *
+ * Memory and ownership.  The caller allocates every buffer, including the
+ * workspace; the library never allocates device memory.  Inputs are only
+ * read.  Outputs are fully overwritten (never accumulated into).  All device
+ * pointers must be 16-byte aligned and must not alias one another.
+ *
+ * Streams.  Each call only enqueues kernels on `stream` (a cudaStream_t
+ * passed as void*, NULL = legacy default stream) and returns; nothing
+ * synchronises the host.  Errors that the host can see (bad sizes, NULL or
+ * misaligned pointers, a workspace that is too small, a failed launch) are
+ * returned at once and nothing is enqueued.  Errors that only the device can
+ * see (a target outside [0, V) that is not ignore_index, a stalled pipeline
+ * stage) are recorded in a status word inside the workspace: read it with
+ * flce_query_status().  Device code never traps.
+ *
+ * Concurrency.  Calls are reentrant; concurrent calls need separate
+ * workspaces.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum flce_status {
+  FLCE_OK = 0,
+  FLCE_EINVAL = 1,        /* NULL pointer, N/H/V < 1, unknown flag          */
+  FLCE_EUNSUPPORTED = 2,  /* H % 8 != 0, pointer not 16-byte aligned,       */
+                          /* size beyond the supported range, no sm_100+ GPU */
+  FLCE_EWORKSPACE = 3,    /* workspace_bytes below the minimum plan          */
+  FLCE_EBADTARGET = 4,    /* (device) a target outside [0,V), not ignored    */
+  FLCE_ETIMEOUT = 5,      /* (device) a pipeline wait ran out of time        */
+  FLCE_ECUDA = 6          /* a CUDA runtime call or launch failed            */
+} flce_status;
+
+/* Reduction flags (bit 0). */
+#define FLCE_REDUCE_MEAN 0x0u  /* mean over non-ignored tokens (default)       */
+#define FLCE_REDUCE_SUM  0x1u  /* unscaled sum; grads without the 1/n_valid   */
+
+/* Description of how a call is carried out for a given workspace size. */
+typedef struct flce_plan_info {
+  int64_t chunk_rows;       /* C: valid tokens processed per chunk            */
+  int64_t max_chunks;       /* chunks launched (ceil(N / C)); empty ones exit  */
+  int64_t logits_row_stride;/* elements per row of the bf16 chunk logits buffer*/
+  int32_t dx_splits;        /* split of the vocabulary for the grad_hidden GEMM*/
+  int32_t vocab_tiles;      /* ceil(V / 256)                                   */
+  size_t workspace_bytes;   /* bytes the plan uses (<= the bytes offered)      */
+} flce_plan_info;
+
+/*
+ * Workspace sizes.
+ * flce_workspace_bytes: the default plan, sized so that the extra device
+ *   memory stays below 5% of the N*V*2 bytes that bf16 logits would take
+ *   (never below one 128-row chunk).
+ * flce_workspace_bytes_for_chunk: the plan with a given chunk size
+ *   (chunk_rows is rounded up to a multiple of 128).
+ * flce_loss_workspace_bytes: the same for the forward-only flce_loss.
+ * Return 0 for invalid sizes.
+ */
+size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags);
+size_t flce_workspace_bytes_for_chunk(int64_t N, int64_t H, int64_t V,
+                                      uint32_t flags, int64_t chunk_rows);
+size_t flce_loss_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags);
+
+/*
+ * The plan flce_fwd_bwd (forward_only = 0) or flce_loss (forward_only = 1)
+ * would use with `workspace_bytes` of workspace: the largest chunk that fits.
+ */
+flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags,
+                      int forward_only, size_t workspace_bytes,
+                      flce_plan_info* out);
+
+/*
+ * Forward + backward in one call.
+ *   hidden       [N,H] bf16 (device)          read
+ *   weight       [V,H] bf16 (device)          read
+ *   targets      [N] int32 (device)           read
+ *   loss         [1] fp32 (device)            written
+ *   n_valid      [1] int32 (device)           written: tokens with t != ignore_index
+ *   row_loss     [N] fp32 (device) or NULL    written: loss_n (unscaled), 0 when ignored
+ *   grad_hidden  [N,H] bf16 (device)          written
+ *   grad_weight  [V,H] fp32 (device)          written
+ *   workspace    device scratch of workspace_bytes (>= flce_workspace_bytes_for_chunk
+ *                with chunk 128); its contents need no initialisation and
+ *                hold the device status word afterwards.
+ * Supported sizes: 1 <= N < 2^31, 8 <= H <= 2^20 with H % 8 == 0,
+ * 1 <= V < 2^31.
+ */
+flce_status flce_fwd_bwd(const void* hidden, const void* weight,
+                         const int32_t* targets, int64_t N, int64_t H,
+                         int64_t V, int32_t ignore_index, uint32_t flags,
+                         float* loss, int32_t* n_valid, float* row_loss,
+                         void* grad_hidden, float* grad_weight,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Forward only: loss (and optionally row_loss) without gradients, 2*N*H*V
+ * flops instead of 6*N*H*V.  Same argument rules as flce_fwd_bwd.
+ */
+flce_status flce_loss(const void* hidden, const void* weight,
+                      const int32_t* targets, int64_t N, int64_t H, int64_t V,
+                      int32_t ignore_index, uint32_t flags, float* loss,
+                      int32_t* n_valid, float* row_loss, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads the device status word of the last call
+ * that used `workspace`: FLCE_OK, FLCE_EBADTARGET or FLCE_ETIMEOUT (or
+ * FLCE_ECUDA if the stream reports an error).
+ */
+flce_status flce_query_status(const void* workspace, void* stream);
+
+/*
+ * Diagnostic: enqueue one kernel that waits on a pipeline barrier nothing
+ * will ever signal, bounded by timeout_ns, so that the timeout path (status
+ * word set to FLCE_ETIMEOUT, kernel returns normally) can be exercised
+ * without hanging the GPU.  Needs >= 256 bytes of workspace.
+ */
+flce_status flce_selftest_timeout(void* workspace, uint64_t timeout_ns,
+                                  void* stream);
+
+/*
+ * Launch profiling (for benchmarks).  Between flce_profile_begin() and
+ * flce_profile_end(), every call records a pair of CUDA events around each
+ * of its tcgen05 GEMM launches on the call's stream and counts every kernel
+ * it launches.  flce_profile_end() synchronises those events and returns, per
+ * GEMM mode (0 = logits, 1 = grad_hidden, 2 = grad_weight), the summed
+ * device time in milliseconds and the number of launches, plus the total
+ * number of kernels launched.  Any output pointer may be NULL.  Profiling is
+ * process-wide and not meant to be used from several threads at once.
+ */
+flce_status flce_profile_begin(void);
+flce_status flce_profile_end(double* gemm_ms /* [3] */, int64_t* gemm_launches /* [3] */,
+                             int64_t* kernel_launches);
+
+/* Static English description of a status code. */
+const char* flce_status_string(flce_status s);
+
+/* Library version, e.g. "0.1.0". */
+const char* flce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H */

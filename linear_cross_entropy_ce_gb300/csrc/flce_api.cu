@@ -1,0 +1,479 @@
+// C ABI of libflce: argument checks, workspace planning, TMA descriptors and
+// the per-chunk launch sequence of the fused linear cross-entropy.
+//
+// Token-major chunking ("efficient-llm-anatomy" README, "Fused cross-entropy
+// computes backward during forward": tokens are processed in chunks and each
+// chunk runs all three matmuls).  For chunk c of C valid tokens:
+//   gather   Xc = rows of X for the chunk's valid tokens
+//   LOGITS   z = Xc W^T; per-tile max / sum-exp, target logit, bf16 z - max
+//   lse_dz   lse per row (fixed-order merge), row loss, dz in place
+//   DX       grad_hidden rows = dz W            (complete per chunk, K = V)
+//   DW       grad_weight (+)= dz^T Xc           (fixed chunk order, fp32)
+// The only buffer that scales with V is the C x V bf16 chunk of logits, so
+// the default plan keeps the workspace below 5% of the N x V bf16 logits.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "flce.h"
+#include "flce_internal.h"
+
+namespace {
+
+using namespace flce;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int major = 0;
+};
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_dev_mu;
+DeviceState g_dev[MAX_DEVICES];
+
+cudaError_t device_state(DeviceState* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+    if ((e = gemm_prepare(dev)) != cudaSuccess) return e;
+    d.ready = true;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+unsigned long long wait_timeout_ns() {
+  static unsigned long long v = [] {
+    const char* s = std::getenv("FLCE_WAIT_TIMEOUT_NS");
+    unsigned long long x = s ? std::strtoull(s, nullptr, 10) : 0ull;
+    return x ? x : 2000000000ull;  // 2 s: far above any legitimate wait
+  }();
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// workspace plan
+// ---------------------------------------------------------------------------
+constexpr int DEFAULT_SMS = 152;
+constexpr int MAX_SPLITS = 8;
+
+struct Plan {
+  long long N = 0, H = 0, V = 0, C = 0, ldz = 0, n_chunks = 0;
+  int nvt = 0, splits = 1, kb_per_split = 0;
+  bool fwd_only = false;
+  size_t o_idx = 0, o_rl = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, o_dxp = 0, total = 0;
+};
+
+inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_only) {
+  Plan p;
+  p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only;
+  p.ldz = cdiv(V, 64) * 64;
+  p.nvt = static_cast<int>(cdiv(V, BN));
+  p.n_chunks = cdiv(N, C);
+  const long long kbt = cdiv(V, BK);
+  if (fwd_only) S = 1;
+  p.kb_per_split = static_cast<int>(cdiv(kbt, S));
+  p.splits = static_cast<int>(cdiv(kbt, p.kb_per_split));
+  size_t off = al256(HDR_WORDS * sizeof(int));
+  p.o_idx = off;  off += al256(size_t(N) * 4);
+  p.o_rl = off;   off += al256(size_t(N) * 4);
+  p.o_xc = off;   off += al256(size_t(C) * H * 2);
+  p.o_tc = off;   off += al256(size_t(C) * 4);
+  p.o_zt = off;   off += al256(size_t(C) * 4);
+  p.o_part = off; off += al256(size_t(C) * p.nvt * 8);
+  if (!fwd_only) {
+    p.o_z = off; off += al256(size_t(C) * p.ldz * 2);
+    if (p.splits > 1) { p.o_dxp = off; off += al256(size_t(p.splits) * C * H * 4); }
+  }
+  p.total = off;
+  return p;
+}
+
+// Vocabulary splits for the grad_hidden GEMM, best wave efficiency first.
+void split_preferences(long long C, long long H, int sms, int* order) {
+  const long long tiles = cdiv(C, BM) * cdiv(H, BN);
+  double eff[MAX_SPLITS + 1];
+  for (int s = 1; s <= MAX_SPLITS; ++s) {
+    const long long u = tiles * s;
+    eff[s] = double(u) / double(cdiv(u, sms) * sms);
+    order[s - 1] = s;
+  }
+  for (int i = 0; i < MAX_SPLITS; ++i)
+    for (int j = i + 1; j < MAX_SPLITS; ++j)
+      if (eff[order[j]] > eff[order[i]] + 1e-9) { int t = order[i]; order[i] = order[j]; order[j] = t; }
+}
+
+long long max_chunk(long long N) { return cdiv(N, BM) * BM; }
+
+// Largest chunk (multiple of 128 rows) whose plan fits in `bytes`.
+bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, int sms, Plan* out) {
+  for (long long C = max_chunk(N); C >= BM; C -= BM) {
+    int order[MAX_SPLITS];
+    split_preferences(C, H, sms, order);
+    for (int i = 0; i < (fwd_only ? 1 : MAX_SPLITS); ++i) {
+      Plan p = layout(N, H, V, C, fwd_only ? 1 : order[i], fwd_only);
+      if (p.total <= bytes) { *out = p; return true; }
+    }
+  }
+  return false;
+}
+
+bool sizes_ok(long long N, long long H, long long V) {
+  return N >= 1 && H >= 8 && V >= 1 && N < (1ll << 31) && V < (1ll << 31) && H <= (1ll << 20) && H % 8 == 0;
+}
+
+size_t default_bytes(long long N, long long H, long long V, bool fwd_only) {
+  if (!sizes_ok(N, H, V)) return 0;
+  const size_t budget = size_t(N) * size_t(V) * 2 / 20;   // 5% of the bf16 logits
+  int sms = DEFAULT_SMS;
+  DeviceState d;
+  if (device_state(&d) == cudaSuccess) sms = d.sms;
+  else cudaGetLastError();
+  Plan p;
+  if (plan_for_bytes(N, H, V, fwd_only, budget, sms, &p)) return p.total;
+  int order[MAX_SPLITS];
+  split_preferences(BM, H, sms, order);
+  return layout(N, H, V, BM, order[0], fwd_only).total;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool make_map(CUtensorMap* m, const void* base, unsigned long long inner, unsigned long long outer,
+              unsigned long long row_bytes, unsigned box_inner, unsigned box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// launch profiling (flce_profile_begin / flce_profile_end)
+// ---------------------------------------------------------------------------
+struct ProfRecord {
+  int mode;
+  cudaEvent_t start, stop;
+};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;  // events available for reuse
+  std::vector<ProfRecord> recs;
+  long long launches = 0;
+};
+
+Profiler& prof() {
+  static Profiler p;
+  return p;
+}
+
+cudaEvent_t prof_event() {
+  Profiler& p = prof();
+  if (!p.pool.empty()) {
+    cudaEvent_t e = p.pool.back();
+    p.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+  return e;
+}
+
+// Launch a GEMM, bracketed by events when profiling is on.
+cudaError_t gemm_launch(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb, int grid, cudaStream_t st) {
+  Profiler& p = prof();
+  std::unique_lock<std::mutex> lk(p.mu);
+  if (!p.on) {
+    lk.unlock();
+    return launch_gemm(g, ta, tb, grid, st);
+  }
+  ProfRecord r{g.mode, prof_event(), prof_event()};
+  if (r.start) cudaEventRecord(r.start, st);
+  cudaError_t e = launch_gemm(g, ta, tb, grid, st);
+  if (r.stop) cudaEventRecord(r.stop, st);
+  if (r.start && r.stop) p.recs.push_back(r);
+  ++p.launches;
+  return e;
+}
+
+void count_launches(long long n) {
+  Profiler& p = prof();
+  std::lock_guard<std::mutex> lk(p.mu);
+  if (p.on) p.launches += n;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+flce_status run(const void* hidden, const void* weight, const int32_t* targets, int64_t N, int64_t H, int64_t V,
+                int32_t ii, uint32_t flags, float* loss, int32_t* n_valid, float* row_loss, void* grad_hidden,
+                float* grad_weight, void* ws, size_t ws_bytes, void* stream, bool fwd_only) {
+  if (!hidden || !weight || !targets || !loss || !n_valid || !ws) return FLCE_EINVAL;
+  if (!fwd_only && (!grad_hidden || !grad_weight)) return FLCE_EINVAL;
+  if (flags & ~FLCE_REDUCE_SUM) return FLCE_EINVAL;
+  if (N < 1 || H < 1 || V < 1) return FLCE_EINVAL;
+  if (!sizes_ok(N, H, V)) return FLCE_EUNSUPPORTED;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(ws) || !aligned4(targets) || !aligned4(loss) ||
+      !aligned4(n_valid) || (row_loss && !aligned4(row_loss)))
+    return FLCE_EUNSUPPORTED;
+  if (!fwd_only && (!aligned16(grad_hidden) || !aligned16(grad_weight))) return FLCE_EUNSUPPORTED;
+
+  DeviceState dev;
+  if (device_state(&dev) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
+  if (dev.major < 10) return FLCE_EUNSUPPORTED;
+  Plan p;
+  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, dev.sms, &p)) return FLCE_EWORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* hdr = at<int>(ws, 0);
+  int* idx = at<int>(ws, p.o_idx);
+  float* rl = at<float>(ws, p.o_rl);
+  uint16_t* xc = at<uint16_t>(ws, p.o_xc);
+  int* tc = at<int>(ws, p.o_tc);
+  float* zt = at<float>(ws, p.o_zt);
+  float2* part = at<float2>(ws, p.o_part);
+  uint16_t* z = fwd_only ? nullptr : at<uint16_t>(ws, p.o_z);
+  float* dxp = (!fwd_only && p.splits > 1) ? at<float>(ws, p.o_dxp) : nullptr;
+
+  CUtensorMap m_xc_k, m_w_k, m_z_k, m_w_mn, m_z_mn, m_xc_mn;
+  const unsigned long long hb = static_cast<unsigned long long>(H) * 2;
+  bool ok = make_map(&m_xc_k, xc, H, p.C, hb, BK, BM) && make_map(&m_w_k, weight, H, V, hb, BK, BN);
+  if (!fwd_only)
+    ok = ok && make_map(&m_z_k, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&m_w_mn, weight, H, V, hb, 64, BK) &&
+         make_map(&m_z_mn, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&m_xc_mn, xc, H, p.C, hb, 64, BK);
+  if (!ok) return FLCE_ECUDA;
+
+  const int reduce_sum = (flags & FLCE_REDUCE_SUM) ? 1 : 0;
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.hdr = hdr;
+  g.status = hdr + HDR_STATUS;
+  g.C = static_cast<int>(p.C);
+  g.H = static_cast<int>(H);
+  g.V = static_cast<int>(V);
+  g.ldz = p.ldz;
+  g.nvt = p.nvt;
+  g.splits = p.splits;
+  g.kb_per_split = p.kb_per_split;
+  g.store_z = fwd_only ? 0 : 1;
+  g.timeout_ns = wait_timeout_ns();
+  g.z = z;
+  g.part = part;
+  g.zt = zt;
+  g.tc = tc;
+  g.idx = idx;
+  g.grad_hidden = static_cast<uint16_t*>(grad_hidden);
+  g.dxp = dxp;
+  g.grad_weight = grad_weight;
+
+  const long long mt = cdiv(p.C, BM), ht = cdiv(H, BN);
+  const int grid_logits = static_cast<int>(std::min<long long>(mt * p.nvt, dev.sms));
+  const int grid_dx = static_cast<int>(std::min<long long>(mt * ht * p.splits, dev.sms));
+  const int grid_dw = static_cast<int>(std::min<long long>(cdiv(V, BM) * ht, dev.sms));
+
+  auto chk = [](cudaError_t e) { return e == cudaSuccess; };
+  const long long aux_per_chunk = 2 + (!fwd_only && p.splits > 1 ? 1 : 0);  // gather, lse_dz, dx_reduce
+  count_launches(2 + (fwd_only ? 0 : 1) + p.n_chunks * aux_per_chunk);      // prep, zero, finalize
+  if (!chk(launch_prep(targets, N, static_cast<int>(V), ii, hdr, idx, n_valid, st))) return FLCE_ECUDA;
+  if (!fwd_only &&
+      !chk(launch_zero_ignored(hdr, idx, N, static_cast<int>(H), static_cast<uint16_t*>(grad_hidden), st)))
+    return FLCE_ECUDA;
+  for (long long c = 0; c < p.n_chunks; ++c) {
+    const long long c0 = c * p.C;
+    g.c0 = c0;
+    if (!chk(launch_gather(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H, xc, tc, st)))
+      return FLCE_ECUDA;
+    g.mode = MODE_LOGITS;
+    if (!chk(gemm_launch(g, m_xc_k, m_w_k, grid_logits, st))) return FLCE_ECUDA;
+    if (!chk(launch_lse_dz(hdr, c0, g.C, g.V, p.ldz, p.nvt, part, zt, tc, rl, z, reduce_sum, fwd_only ? 0 : 1,
+                           st)))
+      return FLCE_ECUDA;
+    if (fwd_only) continue;
+    g.mode = MODE_DX;
+    if (!chk(gemm_launch(g, m_z_k, m_w_mn, grid_dx, st))) return FLCE_ECUDA;
+    if (p.splits > 1 &&
+        !chk(launch_dx_reduce(hdr, idx, c0, g.C, g.H, p.splits, dxp, static_cast<uint16_t*>(grad_hidden), st)))
+      return FLCE_ECUDA;
+    g.mode = MODE_DW;
+    g.accumulate = c > 0 ? 1 : 0;
+    g.first_chunk = c == 0 ? 1 : 0;
+    if (!chk(gemm_launch(g, m_z_mn, m_xc_mn, grid_dw, st))) return FLCE_ECUDA;
+  }
+  if (!chk(launch_finalize(hdr, idx, rl, N, reduce_sum, loss, n_valid, row_loss, st))) return FLCE_ECUDA;
+  return FLCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags) {
+  if (flags & ~FLCE_REDUCE_SUM) return 0;
+  return default_bytes(N, H, V, false);
+}
+
+size_t flce_loss_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags) {
+  if (flags & ~FLCE_REDUCE_SUM) return 0;
+  return default_bytes(N, H, V, true);
+}
+
+size_t flce_workspace_bytes_for_chunk(int64_t N, int64_t H, int64_t V, uint32_t flags, int64_t chunk_rows) {
+  if ((flags & ~FLCE_REDUCE_SUM) || !sizes_ok(N, H, V) || chunk_rows < 1) return 0;
+  long long C = cdiv(chunk_rows, BM) * BM;
+  if (C > max_chunk(N)) C = max_chunk(N);
+  int sms = DEFAULT_SMS;
+  DeviceState d;
+  if (device_state(&d) == cudaSuccess) sms = d.sms;
+  else cudaGetLastError();
+  int order[MAX_SPLITS];
+  split_preferences(C, H, sms, order);
+  return layout(N, H, V, C, order[0], false).total;
+}
+
+flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags, int forward_only, size_t workspace_bytes,
+                      flce_plan_info* out) {
+  if (!out || (flags & ~FLCE_REDUCE_SUM)) return FLCE_EINVAL;
+  if (N < 1 || H < 1 || V < 1) return FLCE_EINVAL;
+  if (!sizes_ok(N, H, V)) return FLCE_EUNSUPPORTED;
+  int sms = DEFAULT_SMS;
+  DeviceState d;
+  if (device_state(&d) == cudaSuccess) sms = d.sms;
+  else cudaGetLastError();
+  Plan p;
+  if (!plan_for_bytes(N, H, V, forward_only != 0, workspace_bytes, sms, &p)) return FLCE_EWORKSPACE;
+  out->chunk_rows = p.C;
+  out->max_chunks = p.n_chunks;
+  out->logits_row_stride = p.ldz;
+  out->dx_splits = p.splits;
+  out->vocab_tiles = p.nvt;
+  out->workspace_bytes = p.total;
+  return FLCE_OK;
+}
+
+flce_status flce_fwd_bwd(const void* hidden, const void* weight, const int32_t* targets, int64_t N, int64_t H,
+                         int64_t V, int32_t ignore_index, uint32_t flags, float* loss, int32_t* n_valid,
+                         float* row_loss, void* grad_hidden, float* grad_weight, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return run(hidden, weight, targets, N, H, V, ignore_index, flags, loss, n_valid, row_loss, grad_hidden,
+             grad_weight, workspace, workspace_bytes, stream, false);
+}
+
+flce_status flce_loss(const void* hidden, const void* weight, const int32_t* targets, int64_t N, int64_t H,
+                      int64_t V, int32_t ignore_index, uint32_t flags, float* loss, int32_t* n_valid,
+                      float* row_loss, void* workspace, size_t workspace_bytes, void* stream) {
+  return run(hidden, weight, targets, N, H, V, ignore_index, flags, loss, n_valid, row_loss, nullptr, nullptr,
+             workspace, workspace_bytes, stream, true);
+}
+
+flce_status flce_query_status(const void* workspace, void* stream) {
+  if (!workspace || !aligned16(workspace)) return FLCE_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
+  int word = 0;
+  if (cudaMemcpy(&word, static_cast<const int*>(workspace) + HDR_STATUS, sizeof(int), cudaMemcpyDeviceToHost) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return FLCE_ECUDA;
+  }
+  if (word & STATUS_TIMEOUT) return FLCE_ETIMEOUT;
+  if (word & STATUS_BADTARGET) return FLCE_EBADTARGET;
+  return FLCE_OK;
+}
+
+flce_status flce_selftest_timeout(void* workspace, uint64_t timeout_ns, void* stream) {
+  if (!workspace || !aligned16(workspace) || timeout_ns == 0 || timeout_ns > 10000000000ull) return FLCE_EINVAL;
+  if (launch_timeout_selftest(static_cast<int*>(workspace), timeout_ns, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return FLCE_ECUDA;
+  return FLCE_OK;
+}
+
+flce_status flce_profile_begin(void) {
+  Profiler& p = prof();
+  std::lock_guard<std::mutex> lk(p.mu);
+  p.on = true;
+  p.launches = 0;
+  return FLCE_OK;
+}
+
+flce_status flce_profile_end(double* gemm_ms, int64_t* gemm_launches, int64_t* kernel_launches) {
+  Profiler& p = prof();
+  std::lock_guard<std::mutex> lk(p.mu);
+  double ms[3] = {0, 0, 0};
+  int64_t cnt[3] = {0, 0, 0};
+  flce_status st = FLCE_OK;
+  for (const ProfRecord& r : p.recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) {
+      cudaGetLastError();
+      st = FLCE_ECUDA;
+    } else if (r.mode >= 0 && r.mode < 3) {
+      ms[r.mode] += t;
+      ++cnt[r.mode];
+    }
+    p.pool.push_back(r.start);
+    p.pool.push_back(r.stop);
+  }
+  p.recs.clear();
+  for (int i = 0; i < 3; ++i) {
+    if (gemm_ms) gemm_ms[i] = ms[i];
+    if (gemm_launches) gemm_launches[i] = cnt[i];
+  }
+  if (kernel_launches) *kernel_launches = p.launches;
+  p.on = false;
+  p.launches = 0;
+  return st;
+}
+
+const char* flce_status_string(flce_status s) {
+  switch (s) {
+    case FLCE_OK: return "ok";
+    case FLCE_EINVAL: return "invalid argument";
+    case FLCE_EUNSUPPORTED: return "unsupported size, alignment or device";
+    case FLCE_EWORKSPACE: return "workspace too small";
+    case FLCE_EBADTARGET: return "target outside [0, V) that is not ignore_index";
+    case FLCE_ETIMEOUT: return "device pipeline wait timed out";
+    case FLCE_ECUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char* flce_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// Bookkeeping and row-wise kernels around the GEMMs of the fused linear
+// cross-entropy:
+//   prep        count the valid tokens (t != ignore_index), build the stable
+//               compaction list (valid rows first, then the others), flag
+//               out-of-range targets ("Alisa's book of LLMs", "implementing
+//               the loss": the loss is a masked sum over the mask count)
+//   zero        grad_hidden rows of ignored tokens = +0.0
+//   gather      copy one chunk of valid hidden rows (and their targets) into
+//               a dense [C, H] tile source; padding rows are zero
+//   lse_dz      merge the per-tile (max, sum exp) pairs of each row into
+//               log-sum-exp in a fixed order, emit loss_n = lse_n - z_t, and
+//               turn the stored shifted logits into dz = (softmax - onehot) * s
+//               in place ("gradient of softmax + CE loss": softmax minus the
+//               one-hot target)
+//   dx_reduce   sum the fp32 partials of a split grad_hidden GEMM in order
+//   finalize    fixed-order sum of the per-row losses, mean over n_valid,
+//               optional per-token loss output
+#include "flce_internal.h"
+#include "flce_ptx.cuh"
+
+namespace flce {
+namespace {
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ int chunk_rows(const int* hdr, long long c0, int C) {
+  const long long rem = static_cast<long long>(hdr[HDR_NVALID]) - c0;
+  return rem <= 0 ? 0 : (rem >= C ? C : static_cast<int>(rem));
+}
+
+__device__ __forceinline__ int round_up_rows(int rows, int C) {
+  const int p = (rows + BM - 1) / BM * BM;
+  return p < C ? p : C;
+}
+
+// Block-wide reductions in a fixed order (xor butterfly inside each warp,
+// then warp 0 over the per-warp results): deterministic for a fixed
+// blockDim.
+template <typename T, typename Op>
+__device__ __forceinline__ T block_reduce(T v, Op op, T identity, T* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32, nw = blockDim.x / 32;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    v = l < nw ? scratch[l] : identity;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (l == 0) scratch[0] = v;
+  }
+  __syncthreads();
+  return scratch[0];
+}
+
+struct MaxOp {
+  __device__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct AddOp {
+  template <typename T>
+  __device__ T operator()(T a, T b) const { return a + b; }
+};
+
+// ---------------------------------------------------------------------------
+constexpr int PREP_THREADS = 1024;
+
+__global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restrict__ t, long long N, int V,
+                                                             int ii, int* hdr, int* __restrict__ idx,
+                                                             int* n_valid_out) {
+  __shared__ int cnt[PREP_THREADS];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  const long long seg = (N + PREP_THREADS - 1) / PREP_THREADS;
+  const long long b = tid * seg;
+  const long long e = b + seg < N ? b + seg : N;
+  int c = 0, mybad = 0;
+  for (long long i = b; i < e; ++i) {
+    const int x = t[i];
+    if (x != ii) {
+      if (x >= 0 && x < V) ++c;
+      else mybad = 1;
+    }
+  }
+  if (tid == 0) bad = 0;
+  cnt[tid] = c;
+  __syncthreads();
+  if (mybad) bad = 1;
+  // inclusive scan of the per-thread counts (Hillis-Steele)
+  for (int off = 1; off < PREP_THREADS; off <<= 1) {
+    const int add = tid >= off ? cnt[tid - off] : 0;
+    __syncthreads();
+    cnt[tid] += add;
+    __syncthreads();
+  }
+  const int total = cnt[PREP_THREADS - 1];
+  int pos = cnt[tid] - c;                                      // valid rows before b
+  long long ipos = total + ((b < N ? b : N) - pos);           // other rows go after all valid ones
+  for (long long i = b; i < e; ++i) {
+    const int x = t[i];
+    if (x != ii && x >= 0 && x < V) idx[pos++] = static_cast<int>(i);
+    else idx[ipos++] = static_cast<int>(i);
+  }
+  if (tid == 0) {
+    hdr[HDR_STATUS] = bad ? STATUS_BADTARGET : 0;
+    hdr[HDR_NVALID] = total;
+    if (n_valid_out) *n_valid_out = total;
+  }
+}
+
+__global__ void zero_ignored_kernel(const int* hdr, const int* __restrict__ idx, long long N, int H,
+                                    uint16_t* __restrict__ gh) {
+  const long long nv = hdr[HDR_NVALID];
+  const long long per_row = H / 8;
+  const long long total = (N - nv) * per_row;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / per_row, c = i - r * per_row;
+    const long long row = idx[nv + r];
+    reinterpret_cast<uint4*>(gh + row * H)[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__global__ void gather_kernel(const uint16_t* __restrict__ X, const int* __restrict__ t, const int* hdr,
+                              const int* __restrict__ idx, long long c0, int C, int H,
+                              uint16_t* __restrict__ xc, int* __restrict__ tc) {
+  const int r = blockIdx.x;
+  const int Cl = chunk_rows(hdr, c0, C);
+  if (r >= round_up_rows(Cl, C)) return;
+  uint4* dst = reinterpret_cast<uint4*>(xc + static_cast<size_t>(r) * H);
+  const int n16 = H / 8;
+  if (r < Cl) {
+    const long long row = idx[c0 + r];
+    const uint4* src = reinterpret_cast<const uint4*>(X + row * H);
+    for (int c = threadIdx.x; c < n16; c += blockDim.x) dst[c] = src[c];
+    if (threadIdx.x == 0) tc[r] = t[row];
+  } else {
+    for (int c = threadIdx.x; c < n16; c += blockDim.x) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) tc[r] = -1;
+  }
+}
+
+constexpr int LSE_THREADS = 256;
+
+__global__ void __launch_bounds__(LSE_THREADS)
+    lse_dz_kernel(const int* hdr, long long c0, int C, int V, long long ldz, int nvt,
+                  const float2* __restrict__ part, const float* __restrict__ zt, const int* __restrict__ tc,
+                  float* __restrict__ rl, uint16_t* __restrict__ z, int reduce_sum, int make_dz) {
+  __shared__ float red[LSE_THREADS / 32];
+  const int r = blockIdx.x;
+  const int Cl = chunk_rows(hdr, c0, C);
+  if (r >= round_up_rows(Cl, C)) return;
+  const int tid = threadIdx.x;
+  uint16_t* zr = z + static_cast<size_t>(r) * ldz;
+  if (r >= Cl) {
+    // padding row of the last chunk: dz = 0 so the grad_weight GEMM sees zeros
+    if (make_dz)
+      for (long long v = tid * 8LL; v < ldz; v += LSE_THREADS * 8LL)
+        *reinterpret_cast<uint4*>(zr + v) = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const float2* pr = part + static_cast<size_t>(r) * nvt;
+  float m = -INFINITY;
+  for (int j = tid; j < nvt; j += LSE_THREADS) m = fmaxf(m, pr[j].x);
+  m = block_reduce(m, MaxOp(), -INFINITY, red);
+  float d = 0.f;
+  for (int j = tid; j < nvt; j += LSE_THREADS) d += pr[j].y * exp2f((pr[j].x - m) * LOG2E);
+  d = block_reduce(d, AddOp(), 0.f, red);
+  const float lse = m + logf(d);
+  if (tid == 0) rl[c0 + r] = lse - zt[r];
+  if (!make_dz) return;
+
+  const long long nv = hdr[HDR_NVALID];
+  const float scale = reduce_sum ? 1.f : 1.f / static_cast<float>(nv);
+  const int tgt = tc[r];
+  for (long long v0 = tid * 8LL; v0 < ldz; v0 += LSE_THREADS * 8LL) {
+    uint4 w = *reinterpret_cast<const uint4*>(zr + v0);
+    if (v0 >= V) {
+      *reinterpret_cast<uint4*>(zr + v0) = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    // the 8 columns lie in one 256-wide tile: z = stored + tile max
+    const float base = pr[v0 / BN].x - lse;
+    uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float s0 = __uint_as_float(in[g] << 16);
+      const float s1 = __uint_as_float(in[g] & 0xFFFF0000u);
+      const long long v = v0 + 2 * g;
+      float d0 = (exp2f((s0 + base) * LOG2E) - (v == tgt ? 1.f : 0.f)) * scale;
+      float d1 = (exp2f((s1 + base) * LOG2E) - (v + 1 == tgt ? 1.f : 0.f)) * scale;
+      if (v >= V) d0 = 0.f;
+      if (v + 1 >= V) d1 = 0.f;
+      out[g] = ptx::pack_bf16x2(d0, d1);
+    }
+    *reinterpret_cast<uint4*>(zr + v0) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+__global__ void dx_reduce_kernel(const int* hdr, const int* __restrict__ idx, long long c0, int C, int H,
+                                 int S, const float* __restrict__ dxp, uint16_t* __restrict__ gh) {
+  const int Cl = chunk_rows(hdr, c0, C);
+  const long long per = H / 4;
+  const long long total = static_cast<long long>(Cl) * per;
+  const size_t plane = static_cast<size_t>(C) * H / 4;
+  const float4* p = reinterpret_cast<const float4*>(dxp);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / per, c = i - r * per;
+    float4 acc = p[r * per + c];
+    for (int s = 1; s < S; ++s) {
+      const float4 q = p[s * plane + r * per + c];
+      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+    }
+    const long long row = idx[c0 + r];
+    reinterpret_cast<uint2*>(gh + row * H)[c] =
+        make_uint2(ptx::pack_bf16x2(acc.x, acc.y), ptx::pack_bf16x2(acc.z, acc.w));
+  }
+}
+
+constexpr int FIN_THREADS = 1024;
+
+__global__ void __launch_bounds__(FIN_THREADS)
+    finalize_kernel(const int* hdr, const int* __restrict__ idx, const float* __restrict__ rl, long long N,
+                    int reduce_sum, float* loss, int* n_valid_out, float* row_loss) {
+  __shared__ double red[FIN_THREADS / 32];
+  const long long nv = hdr[HDR_NVALID];
+  double s = 0.0;
+  for (long long i = threadIdx.x; i < nv; i += FIN_THREADS) s += rl[i];
+  s = block_reduce(s, AddOp(), 0.0, red);
+  if (threadIdx.x == 0) {
+    *loss = nv == 0 ? 0.f : static_cast<float>(reduce_sum ? s : s / static_cast<double>(nv));
+    if (n_valid_out) *n_valid_out = static_cast<int>(nv);
+  }
+  if (row_loss)
+    for (long long i = threadIdx.x; i < N; i += FIN_THREADS) row_loss[idx[i]] = i < nv ? rl[i] : 0.f;
+}
+
+__global__ void timeout_selftest_kernel(int* hdr, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  hdr[HDR_STATUS] = 0;
+  ptx::mbar_init(&bar, 1);
+  ptx::mbar_fence_init();
+  // Phase 0 of a fresh barrier completes only when someone arrives: nobody will.
+  const uint64_t t0 = ptx::global_timer_ns();
+  bool done = false;
+  for (;;) {
+    if (ptx::mbar_test(&bar, 0)) { done = true; break; }
+    if (ptx::global_timer_ns() - t0 > timeout_ns) break;
+  }
+  if (!done) atomicOr(&hdr[HDR_STATUS], STATUS_TIMEOUT);
+}
+
+inline int grid_for(long long work, int threads, int cap) {
+  long long g = (work + threads - 1) / threads;
+  if (g < 1) g = 1;
+  return static_cast<int>(g < cap ? g : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const int* targets, long long N, int V, int ii, int* hdr, int* idx, int* n_valid_out,
+                        cudaStream_t s) {
+  prep_kernel<<<1, PREP_THREADS, 0, s>>>(targets, N, V, ii, hdr, idx, n_valid_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, int H, uint16_t* gh,
+                                cudaStream_t s) {
+  zero_ignored_kernel<<<grid_for(N * (H / 8), 256, 1216), 256, 0, s>>>(hdr, idx, N, H, gh);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t* hidden, const int* targets, const int* hdr, const int* idx,
+                          long long c0, int C, int H, uint16_t* xc, int* tc, cudaStream_t s) {
+  gather_kernel<<<C, 128, 0, s>>>(hidden, targets, hdr, idx, c0, C, H, xc, tc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long ldz, int nvt,
+                          const float2* part, const float* zt, const int* tc, float* rl, uint16_t* z,
+                          int reduce_sum, int make_dz, cudaStream_t s) {
+  lse_dz_kernel<<<C, LSE_THREADS, 0, s>>>(hdr, c0, C, V, ldz, nvt, part, zt, tc, rl, z, reduce_sum, make_dz);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dx_reduce(const int* hdr, const int* idx, long long c0, int C, int H, int splits,
+                             const float* dxp, uint16_t* gh, cudaStream_t s) {
+  dx_reduce_kernel<<<grid_for(static_cast<long long>(C) * (H / 4), 256, 1216), 256, 0, s>>>(
+      hdr, idx, c0, C, H, splits, dxp, gh);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl, long long N, int reduce_sum,
+                            float* loss, int* n_valid_out, float* row_loss, cudaStream_t s) {
+  finalize_kernel<<<1, FIN_THREADS, 0, s>>>(hdr, idx, rl, N, reduce_sum, loss, n_valid_out, row_loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_timeout_selftest(int* hdr, unsigned long long timeout_ns, cudaStream_t s) {
+  timeout_selftest_kernel<<<1, 32, 0, s>>>(hdr, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -1,0 +1,83 @@
+// Internal declarations shared by the CUDA translation units of libflce.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace flce {
+
+// Device status word bits (workspace header word 0).
+constexpr int STATUS_BADTARGET = 1;
+constexpr int STATUS_TIMEOUT = 2;
+
+// Workspace header words.
+constexpr int HDR_STATUS = 0;
+constexpr int HDR_NVALID = 1;
+constexpr int HDR_WORDS = 64;
+
+// GEMM tile shape: one CTA owns a 128 x 256 fp32 accumulator in TMEM and
+// streams K in blocks of 64 bf16 (one 128-byte swizzle row).
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+
+enum GemmMode : int {
+  MODE_LOGITS = 0,  // z = Xc W^T, epilogue: per-tile (max, sum exp), z_t, shifted bf16 logits
+  MODE_DX = 1,      // grad_hidden rows = dz W
+  MODE_DW = 2,      // grad_weight (+)= dz^T Xc
+};
+
+struct GemmArgs {
+  int mode;
+  const int* hdr;       // workspace header (n_valid lives in HDR_NVALID)
+  int* status;          // workspace header word HDR_STATUS
+  long long c0;         // first compacted row of this chunk
+  int C;                // chunk capacity (rows)
+  int H, V;
+  long long ldz;        // row stride (elements) of the chunk logits buffer
+  int nvt;              // ceil(V / BN)
+  int splits;           // DX: number of vocabulary splits
+  int kb_per_split;     // DX: K blocks per split
+  int store_z;          // LOGITS: write the shifted bf16 logits
+  int accumulate;       // DW: add into grad_weight (chunks after the first)
+  int first_chunk;      // DW: chunk 0 (writes zeros when it is empty)
+  unsigned long long timeout_ns;
+  // epilogue operands
+  uint16_t* z;          // [C][ldz] bf16
+  float2* part;         // [C][nvt] (tile max, tile sum of exp)
+  float* zt;            // [C] target logit
+  const int* tc;        // [C] chunk targets (-1 for padding rows)
+  const int* idx;       // [N] compacted row -> token row
+  uint16_t* grad_hidden;// [N][H] bf16
+  float* dxp;           // [splits][C][H] fp32 partials (splits > 1)
+  float* grad_weight;   // [V][H] fp32
+};
+
+int gemm_smem_bytes();
+cudaError_t gemm_prepare(int device);
+cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& ta,
+                        const CUtensorMap& tb, int grid, cudaStream_t s);
+
+// Elementwise / bookkeeping kernels (flce_aux.cu).
+cudaError_t launch_prep(const int* targets, long long N, int V, int ignore_index,
+                        int* hdr, int* idx, int* n_valid_out, cudaStream_t s);
+cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, int H,
+                                uint16_t* grad_hidden, cudaStream_t s);
+cudaError_t launch_gather(const uint16_t* hidden, const int* targets, const int* hdr,
+                          const int* idx, long long c0, int C, int H,
+                          uint16_t* xc, int* tc, cudaStream_t s);
+cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long ldz,
+                          int nvt, const float2* part, const float* zt, const int* tc,
+                          float* rl, uint16_t* z, int reduce_sum, int make_dz,
+                          cudaStream_t s);
+cudaError_t launch_dx_reduce(const int* hdr, const int* idx, long long c0, int C, int H,
+                             int splits, const float* dxp, uint16_t* grad_hidden,
+                             cudaStream_t s);
+cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl,
+                            long long N, int reduce_sum, float* loss, int* n_valid_out,
+                            float* row_loss, cudaStream_t s);
+cudaError_t launch_timeout_selftest(int* hdr, unsigned long long timeout_ns,
+                                    cudaStream_t s);
+
+}  // namespace flce

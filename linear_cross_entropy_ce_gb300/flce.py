@@ -1,0 +1,219 @@
+"""ctypes binding of libflce (argument marshalling only).
+
+Every step of the fused linear cross-entropy runs in the CUDA kernels of
+``libflce.so``; this module only checks tensor types, allocates outputs and
+the workspace through PyTorch's caching allocator, and passes raw device
+pointers and the current CUDA stream to the C ABI declared in
+``include/flce.h``.  There is no fallback: if the library is missing or the
+call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libflce.so")
+
+FLCE_OK, FLCE_EINVAL, FLCE_EUNSUPPORTED, FLCE_EWORKSPACE, FLCE_EBADTARGET, FLCE_ETIMEOUT, FLCE_ECUDA = range(7)
+STATUS_NAMES = {0: "FLCE_OK", 1: "FLCE_EINVAL", 2: "FLCE_EUNSUPPORTED", 3: "FLCE_EWORKSPACE",
+                4: "FLCE_EBADTARGET", 5: "FLCE_ETIMEOUT", 6: "FLCE_ECUDA"}
+REDUCE = {"mean": 0, "sum": 1}
+
+_lib = None
+
+
+class FlceError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{what}: {name} ({_status_string(status)})" if what else name)
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("chunk_rows", ctypes.c_int64), ("max_chunks", ctypes.c_int64),
+                ("logits_row_stride", ctypes.c_int64), ("dx_splits", ctypes.c_int32),
+                ("vocab_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
+
+
+def library() -> ctypes.CDLL:
+    """Load libflce.so (built in-tree by ``linear_cross_entropy_ce_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with linear_cross_entropy_ce_gb300.build.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    i64, u32, i32, sz, vp = ctypes.c_int64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+    lib.flce_workspace_bytes.argtypes = [i64, i64, i64, u32]
+    lib.flce_workspace_bytes.restype = sz
+    lib.flce_loss_workspace_bytes.argtypes = [i64, i64, i64, u32]
+    lib.flce_loss_workspace_bytes.restype = sz
+    lib.flce_workspace_bytes_for_chunk.argtypes = [i64, i64, i64, u32, i64]
+    lib.flce_workspace_bytes_for_chunk.restype = sz
+    lib.flce_plan.argtypes = [i64, i64, i64, u32, ctypes.c_int, sz, ctypes.POINTER(PlanInfo)]
+    lib.flce_plan.restype = ctypes.c_int
+    lib.flce_fwd_bwd.argtypes = [vp, vp, vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_fwd_bwd.restype = ctypes.c_int
+    lib.flce_loss.argtypes = [vp, vp, vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, sz, vp]
+    lib.flce_loss.restype = ctypes.c_int
+    lib.flce_query_status.argtypes = [vp, vp]
+    lib.flce_query_status.restype = ctypes.c_int
+    lib.flce_selftest_timeout.argtypes = [vp, ctypes.c_uint64, vp]
+    lib.flce_selftest_timeout.restype = ctypes.c_int
+    lib.flce_status_string.argtypes = [ctypes.c_int]
+    lib.flce_status_string.restype = ctypes.c_char_p
+    lib.flce_profile_begin.argtypes = []
+    lib.flce_profile_begin.restype = ctypes.c_int
+    lib.flce_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(ctypes.c_int64)]
+    lib.flce_profile_end.restype = ctypes.c_int
+    lib.flce_version.argtypes = []
+    lib.flce_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _status_string(s: int) -> str:
+    try:
+        return library().flce_status_string(int(s)).decode()
+    except Exception:  # pragma: no cover - library not loadable
+        return "?"
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_inputs(hidden, weight, targets):
+    if not (hidden.is_cuda and weight.is_cuda and targets.is_cuda):
+        raise ValueError("hidden, weight and targets must be CUDA tensors")
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight must be bfloat16")
+    if targets.dtype != torch.int32:
+        raise TypeError("targets must be int32")
+    if hidden.dim() != 2 or weight.dim() != 2 or targets.dim() != 1:
+        raise ValueError("expected hidden [N,H], weight [V,H], targets [N]")
+    N, H = hidden.shape
+    V, H2 = weight.shape
+    if H2 != H or targets.shape[0] != N:
+        raise ValueError("shape mismatch")
+    for t in (hidden, weight, targets):
+        if not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    return N, H, V
+
+
+def workspace_bytes(N: int, H: int, V: int, reduction: str = "mean", chunk_rows: Optional[int] = None,
+                    forward_only: bool = False) -> int:
+    lib = library()
+    f = REDUCE[reduction]
+    if forward_only:
+        n = lib.flce_loss_workspace_bytes(N, H, V, f)
+    elif chunk_rows is not None:
+        n = lib.flce_workspace_bytes_for_chunk(N, H, V, f, chunk_rows)
+    else:
+        n = lib.flce_workspace_bytes(N, H, V, f)
+    if n == 0:
+        raise FlceError(FLCE_EINVAL, "workspace size")
+    return int(n)
+
+
+def plan(N: int, H: int, V: int, workspace_bytes: int, forward_only: bool = False,
+         reduction: str = "mean") -> dict:
+    info = PlanInfo()
+    s = library().flce_plan(N, H, V, REDUCE[reduction], int(forward_only), workspace_bytes, ctypes.byref(info))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_plan")
+    return {k: getattr(info, k) for k, _ in PlanInfo._fields_}
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+            reduction: str = "mean", *, workspace: Optional[torch.Tensor] = None,
+            chunk_rows: Optional[int] = None, row_loss: bool = False, out: Optional[dict] = None,
+            stream=None) -> dict:
+    """Loss, n_valid, grad_hidden (bf16 [N,H]) and grad_weight (fp32 [V,H]) in one call."""
+    N, H, V = _check_inputs(hidden, weight, targets)
+    dev = hidden.device
+    if workspace is None:
+        workspace = new_workspace(workspace_bytes(N, H, V, reduction, chunk_rows), dev)
+    o = out if out is not None else {}
+    if "loss" not in o:
+        o["loss"] = torch.empty(1, dtype=torch.float32, device=dev)
+        o["n_valid"] = torch.empty(1, dtype=torch.int32, device=dev)
+        o["grad_hidden"] = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        o["grad_weight"] = torch.empty((V, H), dtype=torch.float32, device=dev)
+        o["row_loss"] = torch.empty(N, dtype=torch.float32, device=dev) if row_loss else None
+    s = library().flce_fwd_bwd(_ptr(hidden), _ptr(weight), _ptr(targets), N, H, V, int(ignore_index),
+                               REDUCE[reduction], _ptr(o["loss"]), _ptr(o["n_valid"]), _ptr(o.get("row_loss")),
+                               _ptr(o["grad_hidden"]), _ptr(o["grad_weight"]), _ptr(workspace),
+                               workspace.numel(), _stream(stream))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_fwd_bwd")
+    o["workspace"] = workspace
+    return o
+
+
+def loss(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+         reduction: str = "mean", *, workspace: Optional[torch.Tensor] = None, row_loss: bool = False,
+         out: Optional[dict] = None, stream=None) -> dict:
+    """Forward only: loss, n_valid and optionally the per-token loss."""
+    N, H, V = _check_inputs(hidden, weight, targets)
+    dev = hidden.device
+    if workspace is None:
+        workspace = new_workspace(workspace_bytes(N, H, V, reduction, forward_only=True), dev)
+    o = out if out is not None else {}
+    if "loss" not in o:
+        o["loss"] = torch.empty(1, dtype=torch.float32, device=dev)
+        o["n_valid"] = torch.empty(1, dtype=torch.int32, device=dev)
+        o["row_loss"] = torch.empty(N, dtype=torch.float32, device=dev) if row_loss else None
+    s = library().flce_loss(_ptr(hidden), _ptr(weight), _ptr(targets), N, H, V, int(ignore_index),
+                            REDUCE[reduction], _ptr(o["loss"]), _ptr(o["n_valid"]), _ptr(o.get("row_loss")),
+                            _ptr(workspace), workspace.numel(), _stream(stream))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_loss")
+    o["workspace"] = workspace
+    return o
+
+
+def query_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the device status of the last call."""
+    return int(library().flce_query_status(_ptr(workspace), _stream(stream)))
+
+
+def selftest_timeout(workspace: torch.Tensor, timeout_ns: int, stream=None) -> int:
+    return int(library().flce_selftest_timeout(_ptr(workspace), int(timeout_ns), _stream(stream)))
+
+
+def profile_begin() -> None:
+    """Record CUDA events around every GEMM launch of the following calls."""
+    library().flce_profile_begin()
+
+
+def profile_end() -> dict:
+    """Synchronise the recorded events; per GEMM mode summed ms and launch counts."""
+    ms = (ctypes.c_double * 3)()
+    n = (ctypes.c_int64 * 3)()
+    total = ctypes.c_int64()
+    s = library().flce_profile_end(ms, n, ctypes.byref(total))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_profile_end")
+    names = ("logits", "grad_hidden", "grad_weight")
+    return {"gemm_ms": dict(zip(names, list(ms))), "gemm_launches": dict(zip(names, list(n))),
+            "kernel_launches": int(total.value)}
+
+
+def version() -> str:
+    return library().flce_version().decode()
