@@ -191,6 +191,8 @@ def main():
     ap.add_argument("--impl", default="flce", choices=["flce", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None, help="override N (small profiling cases)")
+    ap.add_argument("--chunk-rows", type=int, default=None, help="override the default 5%% plan")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "flce":
         args.warmup = 3
@@ -213,6 +215,8 @@ def main():
     flce.library()
 
     base = wl.WORKLOADS[args.workload]
+    if args.tokens:
+        base = base.with_shape(N=args.tokens)
     w = base.with_shape(seed=base.seed + 1000 * rank) if rank else base
     p = wl.make_inputs(w)
     N, H, V = w.N, w.H, w.V
@@ -220,7 +224,7 @@ def main():
     W = torch.from_numpy(p["weight"].view(np.int16)).view(torch.bfloat16).to(dev)
     t = torch.from_numpy(p["targets"]).to(dev)
     nv = int((p["targets"] != -100).sum())
-    ws_bytes = flce.workspace_bytes(N, H, V)
+    ws_bytes = flce.workspace_bytes(N, H, V, chunk_rows=args.chunk_rows)
     plan = flce.plan(N, H, V, ws_bytes)
     ws = flce.new_workspace(ws_bytes, dev)
     out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),

@@ -75,7 +75,7 @@ typedef struct flce_plan_info {
   int64_t chunk_rows;       /* C: valid tokens processed per chunk            */
   int64_t max_chunks;       /* chunks launched (ceil(N / C)); empty ones exit  */
   int64_t logits_row_stride;/* elements per row of the bf16 chunk logits buffer*/
-  int32_t dx_splits;        /* split of the vocabulary for the grad_hidden GEMM*/
+  int32_t gemm_launches_per_chunk; /* 2 (logits; grad_hidden + grad_weight), 1 fwd */
   int32_t vocab_tiles;      /* ceil(V / 256)                                   */
   size_t workspace_bytes;   /* bytes the plan uses (<= the bytes offered)      */
 } flce_plan_info;
@@ -157,9 +157,9 @@ flce_status flce_selftest_timeout(void* workspace, uint64_t timeout_ns,
  * flce_profile_end(), every call records a pair of CUDA events around each
  * of its tcgen05 GEMM launches on the call's stream and counts every kernel
  * it launches.  flce_profile_end() synchronises those events and returns, per
- * GEMM mode (0 = logits, 1 = grad_hidden, 2 = grad_weight), the summed
- * device time in milliseconds and the number of launches, plus the total
- * number of kernels launched.  Any output pointer may be NULL.  Profiling is
+ * GEMM launch kind (0 = logits, 1 = backward: grad_hidden and grad_weight
+ * tiles in one launch, 2 = unused), the summed device time in milliseconds
+ * and the number of launches, plus the total number of kernels launched.  Any output pointer may be NULL.  Profiling is
  * process-wide and not meant to be used from several threads at once.
  */
 flce_status flce_profile_begin(void);

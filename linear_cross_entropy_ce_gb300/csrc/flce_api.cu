@@ -81,71 +81,51 @@ unsigned long long wait_timeout_ns() {
 // ---------------------------------------------------------------------------
 // workspace plan
 // ---------------------------------------------------------------------------
-constexpr int DEFAULT_SMS = 152;
-constexpr int MAX_SPLITS = 8;
-
 struct Plan {
   long long N = 0, H = 0, V = 0, C = 0, ldz = 0, n_chunks = 0;
-  int nvt = 0, splits = 1, kb_per_split = 0;
+  int nvt = 0, n_counters = 0;
   bool fwd_only = false;
-  size_t o_idx = 0, o_rl = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, o_dxp = 0, total = 0;
+  size_t o_idx = 0, o_rl = 0, o_cnt = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, total = 0;
 };
 
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_only) {
+// Workspace layout for chunks of C rows.  Only the bf16 C x V logits buffer
+// (absent for the forward-only call) grows with V.
+Plan layout(long long N, long long H, long long V, long long C, bool fwd_only) {
   Plan p;
   p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only;
   p.ldz = cdiv(V, 64) * 64;
   p.nvt = static_cast<int>(cdiv(V, BN));
   p.n_chunks = cdiv(N, C);
-  const long long kbt = cdiv(V, BK);
-  if (fwd_only) S = 1;
-  p.kb_per_split = static_cast<int>(cdiv(kbt, S));
-  p.splits = static_cast<int>(cdiv(kbt, p.kb_per_split));
+  p.n_counters = static_cast<int>(2 * p.n_chunks);   // one tile counter per GEMM launch
   size_t off = al256(HDR_WORDS * sizeof(int));
   p.o_idx = off;  off += al256(size_t(N) * 4);
   p.o_rl = off;   off += al256(size_t(N) * 4);
+  p.o_cnt = off;  off += al256(size_t(p.n_counters) * 4);
   p.o_xc = off;   off += al256(size_t(C) * H * 2);
   p.o_tc = off;   off += al256(size_t(C) * 4);
   p.o_zt = off;   off += al256(size_t(C) * 4);
   p.o_part = off; off += al256(size_t(C) * p.nvt * 8);
-  if (!fwd_only) {
-    p.o_z = off; off += al256(size_t(C) * p.ldz * 2);
-    if (p.splits > 1) { p.o_dxp = off; off += al256(size_t(p.splits) * C * H * 4); }
-  }
+  if (!fwd_only) { p.o_z = off; off += al256(size_t(C) * p.ldz * 2); }
   p.total = off;
   return p;
-}
-
-// Vocabulary splits for the grad_hidden GEMM, best wave efficiency first.
-void split_preferences(long long C, long long H, int sms, int* order) {
-  const long long tiles = cdiv(C, BM) * cdiv(H, BN);
-  double eff[MAX_SPLITS + 1];
-  for (int s = 1; s <= MAX_SPLITS; ++s) {
-    const long long u = tiles * s;
-    eff[s] = double(u) / double(cdiv(u, sms) * sms);
-    order[s - 1] = s;
-  }
-  for (int i = 0; i < MAX_SPLITS; ++i)
-    for (int j = i + 1; j < MAX_SPLITS; ++j)
-      if (eff[order[j]] > eff[order[i]] + 1e-9) { int t = order[i]; order[i] = order[j]; order[j] = t; }
 }
 
 long long max_chunk(long long N) { return cdiv(N, BM) * BM; }
 
 // Largest chunk (multiple of 128 rows) whose plan fits in `bytes`.
-bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, int sms, Plan* out) {
-  for (long long C = max_chunk(N); C >= BM; C -= BM) {
-    int order[MAX_SPLITS];
-    split_preferences(C, H, sms, order);
-    for (int i = 0; i < (fwd_only ? 1 : MAX_SPLITS); ++i) {
-      Plan p = layout(N, H, V, C, fwd_only ? 1 : order[i], fwd_only);
-      if (p.total <= bytes) { *out = p; return true; }
-    }
+bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, Plan* out) {
+  long long lo = BM, hi = max_chunk(N);
+  if (layout(N, H, V, lo, fwd_only).total > bytes) return false;
+  while (lo < hi) {   // the size grows with C: bisect over multiples of 128
+    const long long mid = ((lo / BM + hi / BM + 1) / 2) * BM;
+    if (layout(N, H, V, mid, fwd_only).total <= bytes) lo = mid;
+    else hi = mid - BM;
   }
-  return false;
+  *out = layout(N, H, V, lo, fwd_only);
+  return true;
 }
 
 bool sizes_ok(long long N, long long H, long long V) {
@@ -155,29 +135,24 @@ bool sizes_ok(long long N, long long H, long long V) {
 size_t default_bytes(long long N, long long H, long long V, bool fwd_only) {
   if (!sizes_ok(N, H, V)) return 0;
   const size_t budget = size_t(N) * size_t(V) * 2 / 20;   // 5% of the bf16 logits
-  int sms = DEFAULT_SMS;
-  DeviceState d;
-  if (device_state(&d) == cudaSuccess) sms = d.sms;
-  else cudaGetLastError();
   Plan p;
-  if (plan_for_bytes(N, H, V, fwd_only, budget, sms, &p)) return p.total;
-  int order[MAX_SPLITS];
-  split_preferences(BM, H, sms, order);
-  return layout(N, H, V, BM, order[0], fwd_only).total;
+  if (plan_for_bytes(N, H, V, fwd_only, budget, &p)) return p.total;
+  return layout(N, H, V, BM, fwd_only).total;             // never below one 128-row chunk
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool make_map(CUtensorMap* m, const void* base, unsigned long long inner, unsigned long long outer,
-              unsigned long long row_bytes, unsigned box_inner, unsigned box_outer) {
+              unsigned long long row_bytes, unsigned box_inner, unsigned box_outer,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -216,16 +191,16 @@ cudaEvent_t prof_event() {
 }
 
 // Launch a GEMM, bracketed by events when profiling is on.
-cudaError_t gemm_launch(const GemmArgs& g, const CUtensorMap& ta, const CUtensorMap& tb, int grid, cudaStream_t st) {
+cudaError_t gemm_launch(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t st) {
   Profiler& p = prof();
   std::unique_lock<std::mutex> lk(p.mu);
   if (!p.on) {
     lk.unlock();
-    return launch_gemm(g, ta, tb, grid, st);
+    return launch_gemm(g, m, grid, st);
   }
   ProfRecord r{g.mode, prof_event(), prof_event()};
   if (r.start) cudaEventRecord(r.start, st);
-  cudaError_t e = launch_gemm(g, ta, tb, grid, st);
+  cudaError_t e = launch_gemm(g, m, grid, st);
   if (r.stop) cudaEventRecord(r.stop, st);
   if (r.start && r.stop) p.recs.push_back(r);
   ++p.launches;
@@ -258,25 +233,29 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   if (device_state(&dev) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
   if (dev.major < 10) return FLCE_EUNSUPPORTED;
   Plan p;
-  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, dev.sms, &p)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, &p)) return FLCE_EWORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* hdr = at<int>(ws, 0);
   int* idx = at<int>(ws, p.o_idx);
   float* rl = at<float>(ws, p.o_rl);
+  int* counters = at<int>(ws, p.o_cnt);
   uint16_t* xc = at<uint16_t>(ws, p.o_xc);
   int* tc = at<int>(ws, p.o_tc);
   float* zt = at<float>(ws, p.o_zt);
   float2* part = at<float2>(ws, p.o_part);
   uint16_t* z = fwd_only ? nullptr : at<uint16_t>(ws, p.o_z);
-  float* dxp = (!fwd_only && p.splits > 1) ? at<float>(ws, p.o_dxp) : nullptr;
 
-  CUtensorMap m_xc_k, m_w_k, m_z_k, m_w_mn, m_z_mn, m_xc_mn;
+  GemmMaps fm, bm;   // forward (logits) and backward (dX + dW) launches
+  std::memset(&fm, 0, sizeof(fm));
+  std::memset(&bm, 0, sizeof(bm));
   const unsigned long long hb = static_cast<unsigned long long>(H) * 2;
-  bool ok = make_map(&m_xc_k, xc, H, p.C, hb, BK, BM) && make_map(&m_w_k, weight, H, V, hb, BK, BN);
+  bool ok = make_map(&fm.a0, xc, H, p.C, hb, BK, BM) && make_map(&fm.b0, weight, H, V, hb, BK, BN);
   if (!fwd_only)
-    ok = ok && make_map(&m_z_k, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&m_w_mn, weight, H, V, hb, 64, BK) &&
-         make_map(&m_z_mn, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&m_xc_mn, xc, H, p.C, hb, 64, BK);
+    ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, weight, H, V, hb, 64, BK) &&
+         make_map(&bm.a1, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&bm.b1, xc, H, p.C, hb, 64, BK) &&
+         make_map(&bm.out, grad_weight, H, V, static_cast<unsigned long long>(H) * 4, 32, BM,
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
   if (!ok) return FLCE_ECUDA;
 
   const int reduce_sum = (flags & FLCE_REDUCE_SUM) ? 1 : 0;
@@ -289,8 +268,6 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   g.V = static_cast<int>(V);
   g.ldz = p.ldz;
   g.nvt = p.nvt;
-  g.splits = p.splits;
-  g.kb_per_split = p.kb_per_split;
   g.store_z = fwd_only ? 0 : 1;
   g.timeout_ns = wait_timeout_ns();
   g.z = z;
@@ -299,18 +276,16 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   g.tc = tc;
   g.idx = idx;
   g.grad_hidden = static_cast<uint16_t*>(grad_hidden);
-  g.dxp = dxp;
   g.grad_weight = grad_weight;
 
   const long long mt = cdiv(p.C, BM), ht = cdiv(H, BN);
   const int grid_logits = static_cast<int>(std::min<long long>(mt * p.nvt, dev.sms));
-  const int grid_dx = static_cast<int>(std::min<long long>(mt * ht * p.splits, dev.sms));
-  const int grid_dw = static_cast<int>(std::min<long long>(cdiv(V, BM) * ht, dev.sms));
+  const int grid_bwd = static_cast<int>(std::min<long long>(mt * ht + cdiv(V, BM) * ht, dev.sms));
 
   auto chk = [](cudaError_t e) { return e == cudaSuccess; };
-  const long long aux_per_chunk = 2 + (!fwd_only && p.splits > 1 ? 1 : 0);  // gather, lse_dz, dx_reduce
-  count_launches(2 + (fwd_only ? 0 : 1) + p.n_chunks * aux_per_chunk);      // prep, zero, finalize
-  if (!chk(launch_prep(targets, N, static_cast<int>(V), ii, hdr, idx, n_valid, st))) return FLCE_ECUDA;
+  count_launches(2 + (fwd_only ? 0 : 1) + p.n_chunks * 2);   // prep, zero, finalize; gather + lse_dz per chunk
+  if (!chk(launch_prep(targets, N, static_cast<int>(V), ii, hdr, idx, n_valid, counters, p.n_counters, st)))
+    return FLCE_ECUDA;
   if (!fwd_only &&
       !chk(launch_zero_ignored(hdr, idx, N, static_cast<int>(H), static_cast<uint16_t*>(grad_hidden), st)))
     return FLCE_ECUDA;
@@ -320,20 +295,17 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
     if (!chk(launch_gather(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H, xc, tc, st)))
       return FLCE_ECUDA;
     g.mode = MODE_LOGITS;
-    if (!chk(gemm_launch(g, m_xc_k, m_w_k, grid_logits, st))) return FLCE_ECUDA;
+    g.counter = counters + 2 * c;
+    if (!chk(gemm_launch(g, fm, grid_logits, st))) return FLCE_ECUDA;
     if (!chk(launch_lse_dz(hdr, c0, g.C, g.V, p.ldz, p.nvt, part, zt, tc, rl, z, reduce_sum, fwd_only ? 0 : 1,
                            st)))
       return FLCE_ECUDA;
     if (fwd_only) continue;
-    g.mode = MODE_DX;
-    if (!chk(gemm_launch(g, m_z_k, m_w_mn, grid_dx, st))) return FLCE_ECUDA;
-    if (p.splits > 1 &&
-        !chk(launch_dx_reduce(hdr, idx, c0, g.C, g.H, p.splits, dxp, static_cast<uint16_t*>(grad_hidden), st)))
-      return FLCE_ECUDA;
-    g.mode = MODE_DW;
+    g.mode = MODE_BWD;
+    g.counter = counters + 2 * c + 1;
     g.accumulate = c > 0 ? 1 : 0;
     g.first_chunk = c == 0 ? 1 : 0;
-    if (!chk(gemm_launch(g, m_z_mn, m_xc_mn, grid_dw, st))) return FLCE_ECUDA;
+    if (!chk(gemm_launch(g, bm, grid_bwd, st))) return FLCE_ECUDA;
   }
   if (!chk(launch_finalize(hdr, idx, rl, N, reduce_sum, loss, n_valid, row_loss, st))) return FLCE_ECUDA;
   return FLCE_OK;
@@ -357,13 +329,7 @@ size_t flce_workspace_bytes_for_chunk(int64_t N, int64_t H, int64_t V, uint32_t 
   if ((flags & ~FLCE_REDUCE_SUM) || !sizes_ok(N, H, V) || chunk_rows < 1) return 0;
   long long C = cdiv(chunk_rows, BM) * BM;
   if (C > max_chunk(N)) C = max_chunk(N);
-  int sms = DEFAULT_SMS;
-  DeviceState d;
-  if (device_state(&d) == cudaSuccess) sms = d.sms;
-  else cudaGetLastError();
-  int order[MAX_SPLITS];
-  split_preferences(C, H, sms, order);
-  return layout(N, H, V, C, order[0], false).total;
+  return layout(N, H, V, C, false).total;
 }
 
 flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags, int forward_only, size_t workspace_bytes,
@@ -371,16 +337,12 @@ flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags, int forwa
   if (!out || (flags & ~FLCE_REDUCE_SUM)) return FLCE_EINVAL;
   if (N < 1 || H < 1 || V < 1) return FLCE_EINVAL;
   if (!sizes_ok(N, H, V)) return FLCE_EUNSUPPORTED;
-  int sms = DEFAULT_SMS;
-  DeviceState d;
-  if (device_state(&d) == cudaSuccess) sms = d.sms;
-  else cudaGetLastError();
   Plan p;
-  if (!plan_for_bytes(N, H, V, forward_only != 0, workspace_bytes, sms, &p)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, forward_only != 0, workspace_bytes, &p)) return FLCE_EWORKSPACE;
   out->chunk_rows = p.C;
   out->max_chunks = p.n_chunks;
   out->logits_row_stride = p.ldz;
-  out->dx_splits = p.splits;
+  out->gemm_launches_per_chunk = forward_only ? 1 : 2;
   out->vocab_tiles = p.nvt;
   out->workspace_bytes = p.total;
   return FLCE_OK;

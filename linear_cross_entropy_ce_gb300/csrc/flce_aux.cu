@@ -12,7 +12,6 @@
 //               turn the stored shifted logits into dz = (softmax - onehot) * s
 //               in place ("gradient of softmax + CE loss": softmax minus the
 //               one-hot target)
-//   dx_reduce   sum the fp32 partials of a split grad_hidden GEMM in order
 //   finalize    fixed-order sum of the per-row losses, mean over n_valid,
 //               optional per-token loss output
 #include "flce_internal.h"
@@ -67,7 +66,7 @@ constexpr int PREP_THREADS = 1024;
 
 __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restrict__ t, long long N, int V,
                                                              int ii, int* hdr, int* __restrict__ idx,
-                                                             int* n_valid_out) {
+                                                             int* n_valid_out, int* counters, int n_counters) {
   __shared__ int cnt[PREP_THREADS];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -83,6 +82,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restric
     }
   }
   if (tid == 0) bad = 0;
+  for (int i = tid; i < n_counters; i += PREP_THREADS) counters[i] = 0;  // tile counters of the GEMMs
   cnt[tid] = c;
   __syncthreads();
   if (mybad) bad = 1;
@@ -198,27 +198,6 @@ __global__ void __launch_bounds__(LSE_THREADS)
   }
 }
 
-__global__ void dx_reduce_kernel(const int* hdr, const int* __restrict__ idx, long long c0, int C, int H,
-                                 int S, const float* __restrict__ dxp, uint16_t* __restrict__ gh) {
-  const int Cl = chunk_rows(hdr, c0, C);
-  const long long per = H / 4;
-  const long long total = static_cast<long long>(Cl) * per;
-  const size_t plane = static_cast<size_t>(C) * H / 4;
-  const float4* p = reinterpret_cast<const float4*>(dxp);
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = i / per, c = i - r * per;
-    float4 acc = p[r * per + c];
-    for (int s = 1; s < S; ++s) {
-      const float4 q = p[s * plane + r * per + c];
-      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
-    }
-    const long long row = idx[c0 + r];
-    reinterpret_cast<uint2*>(gh + row * H)[c] =
-        make_uint2(ptx::pack_bf16x2(acc.x, acc.y), ptx::pack_bf16x2(acc.z, acc.w));
-  }
-}
-
 constexpr int FIN_THREADS = 1024;
 
 __global__ void __launch_bounds__(FIN_THREADS)
@@ -262,8 +241,8 @@ inline int grid_for(long long work, int threads, int cap) {
 }  // namespace
 
 cudaError_t launch_prep(const int* targets, long long N, int V, int ii, int* hdr, int* idx, int* n_valid_out,
-                        cudaStream_t s) {
-  prep_kernel<<<1, PREP_THREADS, 0, s>>>(targets, N, V, ii, hdr, idx, n_valid_out);
+                        int* counters, int n_counters, cudaStream_t s) {
+  prep_kernel<<<1, PREP_THREADS, 0, s>>>(targets, N, V, ii, hdr, idx, n_valid_out, counters, n_counters);
   return cudaGetLastError();
 }
 
@@ -283,13 +262,6 @@ cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long 
                           const float2* part, const float* zt, const int* tc, float* rl, uint16_t* z,
                           int reduce_sum, int make_dz, cudaStream_t s) {
   lse_dz_kernel<<<C, LSE_THREADS, 0, s>>>(hdr, c0, C, V, ldz, nvt, part, zt, tc, rl, z, reduce_sum, make_dz);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dx_reduce(const int* hdr, const int* idx, long long c0, int C, int H, int splits,
-                             const float* dxp, uint16_t* gh, cudaStream_t s) {
-  dx_reduce_kernel<<<grid_for(static_cast<long long>(C) * (H / 4), 256, 1216), 256, 0, s>>>(
-      hdr, idx, c0, C, H, splits, dxp, gh);
   return cudaGetLastError();
 }
 

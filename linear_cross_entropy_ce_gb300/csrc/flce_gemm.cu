@@ -1,4 +1,4 @@
-// Persistent tcgen05 GEMM with the three epilogues of the fused linear
+// Persistent tcgen05 GEMM with the epilogues of the fused linear
 // cross-entropy ("efficient-llm-anatomy" README, "Fused cross-entropy
 // computes backward during forward": per token chunk, logits = X W^T, then
 // grad_input and grad_weight from the softmax of those logits).
@@ -8,15 +8,19 @@
 //                and sum exp(z - m) (one step of the online softmax of
 //                "Alisa's book of LLMs", "Numerical stability and other
 //                tricks"), the target logit, and z - m stored as bf16.
-//   MODE_DX      dX = dz W            A = dz [C,V] K-major,  B = W [V,H] MN-major
-//                epilogue: bf16 rows of grad_hidden (scattered to token rows)
-//                or fp32 partials when the vocabulary is split.
-//   MODE_DW      dW (+)= dz^T Xc      A = dz^T (MN-major view of dz), B = Xc MN-major
-//                epilogue: fp32 grad_weight, added in fixed chunk order.
+//   MODE_BWD     the two consumers of dz in one launch:
+//     dX units   dX = dz W            A = dz [C,V] K-major,  B = W [V,H] MN-major
+//                epilogue: bf16 rows of grad_hidden, scattered to token rows.
+//     dW units   dW (+)= dz^T Xc      A = dz^T (MN-major view of dz), B = Xc MN-major
+//                epilogue: fp32 tile staged in shared memory and written by a
+//                TMA store (first chunk) or a TMA reduce-add (later chunks),
+//                so the fp32 accumulation happens in L2 in fixed chunk order.
 //
-// One CTA per SM, 192 threads: warp 0 issues TMA loads into a 4-stage shared
-// memory ring, warp 1 allocates TMEM and one lane issues tcgen05.mma
-// (128 x 256 x 16, bf16 -> fp32), warps 2-5 drain the two TMEM accumulators
+// One CTA per SM, 192 threads: warp 0 claims tiles from a global counter
+// (dynamic scheduling, so the long grad_hidden tiles and the short
+// grad_weight tiles share the SMs) and issues TMA loads into a 4-stage shared
+// memory ring; warp 1 allocates TMEM and one lane issues tcgen05.mma
+// (128 x 256 x 16, bf16 -> fp32); warps 2-5 drain the two TMEM accumulators
 // (double buffered, 2 x 256 columns) so the epilogue of one tile overlaps the
 // main loop of the next.  Every wait is bounded: on time-out the CTA raises
 // an abort flag, lets copies in flight land, frees TMEM and returns, and the
@@ -31,8 +35,11 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STG_BYTES = BM * 32 * 4;   // one 128 x 32 fp32 slice of a grad_weight tile
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
+constexpr int SCHED_SLOTS = 4;
+constexpr uint32_t EPI_BAR = 1;          // named barrier of the epilogue warps
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MN_BLOCK_BYTES = 64 * 128; // 64 K rows x 128 B (64 bf16 along M or N)
 constexpr float LOG2E = 1.4426950408889634f;
@@ -42,12 +49,17 @@ struct Ctl {
   uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t sfull[SCHED_SLOTS];
+  uint64_t sempty[SCHED_SLOTS];
   uint64_t mma_done;
+  int sunit[SCHED_SLOTS];
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + ((sizeof(Ctl) + 127) / 128) * 128;
+constexpr int CTL_BYTES = ((sizeof(Ctl) + 255) / 256) * 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STG_BYTES + CTL_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Bounded wait on an mbarrier phase.  Gives up (returning false) when the
 // CTA's abort flag is raised by another role, or after timeout_ns, in which
@@ -69,9 +81,11 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Ctl* ctl
 }
 
 struct Shape {
-  int Cl;        // valid rows in this chunk
-  int mt, nt;    // tiles along M and N
-  int kbt;       // K blocks in total
+  int Cl;         // valid rows in this chunk
+  int mt, nt;     // LOGITS: tiles along M and N; BWD: dX tiles along M and N
+  int kbt;        // LOGITS: K blocks
+  int n_dx;       // BWD: number of dX units (they come first)
+  int dw_mt;      // BWD: dW tiles along M (vocabulary)
   int units;
 };
 
@@ -80,45 +94,43 @@ __device__ __forceinline__ Shape make_shape(const GemmArgs& a) {
   const long long nv = a.hdr[HDR_NVALID];
   const long long rem = nv - a.c0;
   s.Cl = rem <= 0 ? 0 : (rem >= a.C ? a.C : static_cast<int>(rem));
+  s.mt = (s.Cl + BM - 1) / BM;
   if (a.mode == MODE_LOGITS) {
-    s.mt = (s.Cl + BM - 1) / BM;
     s.nt = a.nvt;
     s.kbt = (a.H + BK - 1) / BK;
+    s.n_dx = 0;
+    s.dw_mt = 0;
     s.units = s.mt * s.nt;
-  } else if (a.mode == MODE_DX) {
-    s.mt = (s.Cl + BM - 1) / BM;
-    s.nt = (a.H + BN - 1) / BN;
-    s.kbt = (a.V + BK - 1) / BK;
-    s.units = s.mt * s.nt * a.splits;
   } else {
-    s.mt = (a.V + BM - 1) / BM;
     s.nt = (a.H + BN - 1) / BN;
-    s.kbt = (s.Cl + BK - 1) / BK;
-    s.units = s.Cl > 0 ? s.mt * s.nt : 0;
+    s.kbt = 0;
+    s.n_dx = s.mt * s.nt;
+    s.dw_mt = (a.V + BM - 1) / BM;
+    s.units = s.Cl > 0 ? s.n_dx + s.dw_mt * s.nt : 0;
   }
   return s;
 }
 
+enum UnitKind : int { U_LOGITS = 0, U_DX = 1, U_DW = 2 };
+
 struct Unit {
-  int m0, n0, ntile, split, kb0, kb1;
+  int kind, m0, n0, ntile, kb1;
 };
 
 // Tile order: LOGITS walks M fastest so the CTAs in flight share one W tile;
-// DX and DW walk N fastest so they share one slab of dz.
+// dX and dW walk N fastest so they share one slab of dz.
 __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const Shape& s, int u) {
   Unit t;
   if (a.mode == MODE_LOGITS) {
     const int m = u % s.mt, n = u / s.mt;
-    t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.split = 0; t.kb0 = 0; t.kb1 = s.kbt;
-  } else if (a.mode == MODE_DX) {
-    const int n = u % s.nt, rest = u / s.nt;
-    const int m = rest % s.mt, sp = rest / s.mt;
-    t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.split = sp;
-    t.kb0 = sp * a.kb_per_split;
-    t.kb1 = min(s.kbt, t.kb0 + a.kb_per_split);
-  } else {
+    t.kind = U_LOGITS; t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.kb1 = s.kbt;
+  } else if (u < s.n_dx) {
     const int n = u % s.nt, m = u / s.nt;
-    t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.split = 0; t.kb0 = 0; t.kb1 = s.kbt;
+    t.kind = U_DX; t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.kb1 = (a.V + BK - 1) / BK;
+  } else {
+    const int w = u - s.n_dx;
+    const int n = w % s.nt, m = w / s.nt;
+    t.kind = U_DW; t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.kb1 = (s.Cl + BK - 1) / BK;
   }
   return t;
 }
@@ -174,8 +186,7 @@ __device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, co
   }
 }
 
-__device__ __forceinline__ void epi_dx(const GemmArgs& a, const Shape& s, const Unit& t, uint32_t tbase,
-                                       int r) {
+__device__ __forceinline__ void epi_dx(const GemmArgs& a, const Shape& s, const Unit& t, uint32_t tbase, int r) {
   const int grow = t.m0 + r;
   const bool rv = grow < s.Cl;
   const long long tok = rv ? a.idx[a.c0 + grow] : 0;
@@ -186,64 +197,64 @@ __device__ __forceinline__ void epi_dx(const GemmArgs& a, const Shape& s, const 
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
     if (!rv) continue;
-    if (a.splits == 1) {
-      uint16_t* dst = a.grad_hidden + tok * a.H + h;
+    uint16_t* dst = a.grad_hidden + tok * a.H + h;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        if (h + g * 8 < a.H) {
-          const float* q = v + 8 * g;
-          *reinterpret_cast<uint4*>(dst + 8 * g) =
-              make_uint4(ptx::pack_bf16x2(q[0], q[1]), ptx::pack_bf16x2(q[2], q[3]),
-                         ptx::pack_bf16x2(q[4], q[5]), ptx::pack_bf16x2(q[6], q[7]));
-        }
+    for (int g = 0; g < 4; ++g) {
+      if (h + g * 8 < a.H) {
+        const float* q = v + 8 * g;
+        *reinterpret_cast<uint4*>(dst + 8 * g) =
+            make_uint4(ptx::pack_bf16x2(q[0], q[1]), ptx::pack_bf16x2(q[2], q[3]), ptx::pack_bf16x2(q[4], q[5]),
+                       ptx::pack_bf16x2(q[6], q[7]));
       }
-    } else {
-      float* dst = a.dxp + (static_cast<size_t>(t.split) * a.C + grow) * a.H + h;
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        if (h + g * 4 < a.H)
-          *reinterpret_cast<float4*>(dst + 4 * g) = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
     }
   }
 }
 
-__device__ __forceinline__ void epi_dw(const GemmArgs& a, const Unit& t, uint32_t tbase, int r) {
-  const int vrow = t.m0 + r;
-  const bool rv = vrow < a.V;
+// grad_weight tile: 32-column slices go TMEM -> registers -> shared memory
+// (128-byte swizzled rows, conflict-free) -> TMA store or reduce-add.  Two
+// staging buffers alternate; `leader` owns the bulk-group bookkeeping.
+__device__ __forceinline__ void epi_dw(const GemmArgs& a, const GemmMaps* maps, const Unit& t, uint32_t tbase,
+                                       int r, bool leader, uint8_t* stg, uint32_t& stg_count) {
+  (void)maps;
 #pragma unroll 1
   for (int j = 0; j < BN / 32; ++j) {
     const int h = t.n0 + j * 32;
-    if (h >= a.H) break;  // warp-uniform
+    if (h >= a.H) break;  // uniform over the epilogue warps
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
-    if (!rv) continue;
-    float* dst = a.grad_weight + static_cast<size_t>(vrow) * a.H + h;
+    uint8_t* buf = stg + (stg_count & 1u) * STG_BYTES;
+    if (leader) ptx::bulk_wait_read_1();          // the store that last used `buf` has read it
+    ptx::named_bar_sync(EPI_BAR, EPI_THREADS);
+    uint8_t* row = buf + r * 128;
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      if (h + g * 4 < a.H) {
-        float4 o = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-        if (a.accumulate) {
-          const float4 p = *reinterpret_cast<const float4*>(dst + 4 * g);
-          o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
-        }
-        *reinterpret_cast<float4*>(dst + 4 * g) = o;
-      }
+    for (int g = 0; g < 8; ++g)
+      *reinterpret_cast<float4*>(row + ((g ^ (r & 7)) << 4)) =
+          make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(EPI_BAR, EPI_THREADS);
+    if (leader) {
+      if (a.accumulate)
+        ptx::tma_reduce_add_2d(&maps->out, buf, h, t.m0);
+      else
+        ptx::tma_store_2d(&maps->out, buf, h, t.m0);
+      ptx::bulk_commit();
     }
+    ++stg_count;
   }
 }
 
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const GemmArgs a) {
+    flce_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* stg = smem + STAGES * STAGE_BYTES;
+  Ctl* ctl = reinterpret_cast<Ctl*>(stg + 2 * STG_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   const Shape s = make_shape(a);
-  if (a.mode == MODE_DW && s.Cl == 0) {
+  if (a.mode == MODE_BWD && s.Cl == 0) {
     // Empty first chunk (no valid token at all): grad_weight is zero.
     if (a.first_chunk) {
       const size_t n4 = static_cast<size_t>(a.V) * a.H / 4;
@@ -254,7 +265,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     return;
   }
-  if (static_cast<int>(blockIdx.x) >= s.units) return;
+  if (s.units == 0) return;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -265,11 +276,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(&ctl->tfull[i], 1);
       ptx::mbar_init(&ctl->tempty[i], EPI_THREADS);
     }
+    for (int i = 0; i < SCHED_SLOTS; ++i) {
+      ptx::mbar_init(&ctl->sfull[i], 1);
+      ptx::mbar_init(&ctl->sempty[i], 1 + EPI_THREADS);
+    }
     ptx::mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
     ptx::mbar_fence_init();
-    ptx::tma_prefetch_desc(&tmap_a);
-    ptx::tma_prefetch_desc(&tmap_b);
+    ptx::tma_prefetch_desc(&maps.a0);
+    ptx::tma_prefetch_desc(&maps.b0);
+    if (a.mode == MODE_BWD) {
+      ptx::tma_prefetch_desc(&maps.a1);
+      ptx::tma_prefetch_desc(&maps.b1);
+      ptx::tma_prefetch_desc(&maps.out);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
@@ -280,43 +300,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const uint64_t to = a.timeout_ns;
-  const int a_mn = a.mode == MODE_DW ? 1 : 0;
-  const int b_mn = a.mode == MODE_LOGITS ? 0 : 1;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
-    uint32_t stage = 0, phase = 0;
+    // ---------------- scheduler + TMA producer ----------------
+    uint32_t stage = 0, phase = 0, sslot = 0, sphase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+    for (;;) {
+      if (!wait_phase(&ctl->sempty[sslot], sphase ^ 1u, ctl, to, true)) { ok = false; break; }
+      int u = atomicAdd(a.counter, 1);
+      if (u >= s.units) u = -1;
+      ctl->sunit[sslot] = u;
+      ptx::mbar_arrive(&ctl->sfull[sslot]);
+      if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
+      if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
-      for (int kb = t.kb0; kb < t.kb1; ++kb) {
+      for (int kb = 0; kb < t.kb1; ++kb) {
         if (!wait_phase(&ctl->empty[stage], phase ^ 1u, ctl, to, true)) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         uint64_t* fb = &ctl->full[stage];
         ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
         const int k0 = kb * BK;
-        if (a.mode == MODE_LOGITS) {
-          ptx::tma_load_2d(sa, &tmap_a, fb, k0, t.m0);      // Xc rows m0.., cols k0..
-          ptx::tma_load_2d(sb, &tmap_b, fb, k0, t.n0);      // W rows n0.., cols k0..
-        } else if (a.mode == MODE_DX) {
-          ptx::tma_load_2d(sa, &tmap_a, fb, k0, t.m0);      // dz rows m0.., vocab k0..
+        if (t.kind == U_LOGITS) {
+          ptx::tma_load_2d(sa, &maps.a0, fb, k0, t.m0);      // Xc rows m0.., cols k0..
+          ptx::tma_load_2d(sb, &maps.b0, fb, k0, t.n0);      // W rows n0.., cols k0..
+        } else if (t.kind == U_DX) {
+          ptx::tma_load_2d(sa, &maps.a0, fb, k0, t.m0);      // dz rows m0.., vocab k0..
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)                   // W rows k0.., cols n0+64j..
-            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &tmap_b, fb, t.n0 + 64 * j, k0);
+          for (int j = 0; j < BN / 64; ++j)                    // W rows k0.., cols n0+64j..
+            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &maps.b0, fb, t.n0 + 64 * j, k0);
         } else {
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j)                   // dz rows k0.., vocab m0+64j..
-            ptx::tma_load_2d(sa + j * MN_BLOCK_BYTES, &tmap_a, fb, t.m0 + 64 * j, k0);
+          for (int j = 0; j < BM / 64; ++j)                    // dz rows k0.., vocab m0+64j..
+            ptx::tma_load_2d(sa + j * MN_BLOCK_BYTES, &maps.a1, fb, t.m0 + 64 * j, k0);
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)                   // Xc rows k0.., cols n0+64j..
-            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &tmap_b, fb, t.n0 + 64 * j, k0);
+          for (int j = 0; j < BN / 64; ++j)                    // Xc rows k0.., cols n0+64j..
+            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &maps.b1, fb, t.n0 + 64 * j, k0);
         }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
+      if (!ok) break;
     }
     if (!ok) {
       // let the copies already in flight land before the CTA exits
@@ -325,17 +351,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, a_mn, b_mn);
-    const uint32_t a_lbo = a_mn ? MN_BLOCK_BYTES : 16, b_lbo = b_mn ? MN_BLOCK_BYTES : 16;
-    const uint32_t a_kstep = a_mn ? 16 * 128 : 32, b_kstep = b_mn ? 16 * 128 : 32;
-    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, sslot = 0, sphase = 0;
+    for (;;) {
+      if (!wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true)) break;
+      const int u = ctl->sunit[sslot];
+      ptx::mbar_arrive(&ctl->sempty[sslot]);
+      if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
+      if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
-      if (!wait_phase(&ctl->tempty[acc], acc_phase ^ 1u, ctl, to, true)) { ok = false; break; }
+      const int a_mn = t.kind == U_DW ? 1 : 0;
+      const int b_mn = t.kind == U_LOGITS ? 0 : 1;
+      const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, a_mn, b_mn);
+      const uint32_t a_lbo = a_mn ? MN_BLOCK_BYTES : 16, b_lbo = b_mn ? MN_BLOCK_BYTES : 16;
+      const uint32_t a_kstep = a_mn ? 16 * 128 : 32, b_kstep = b_mn ? 16 * 128 : 32;
+      if (!wait_phase(&ctl->tempty[acc], acc_phase ^ 1u, ctl, to, true)) break;
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem + acc * BN;
-      for (int kb = t.kb0; kb < t.kb1; ++kb) {
+      bool ok = true;
+      for (int kb = 0; kb < t.kb1; ++kb) {
         if (!wait_phase(&ctl->full[stage], phase, ctl, to, true)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
@@ -344,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint64_t ad = ptx::smem_desc_sw128(sa + kk * a_kstep, a_lbo, 1024);
           const uint64_t bd = ptx::smem_desc_sw128(sb + kk * b_kstep, b_lbo, 1024);
-          ptx::umma_bf16(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+          ptx::umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
         }
         ptx::umma_commit(&ctl->empty[stage]);   // frees the smem slot when these MMAs finish
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -360,23 +393,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------- epilogue ----------------
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;        // accumulator row
-    uint32_t acc = 0, acc_phase = 0;
-    for (int u = blockIdx.x; u < s.units; u += gridDim.x) {
+    const bool leader = warp == 2 && lane == 0;
+    uint32_t acc = 0, acc_phase = 0, sslot = 0, sphase = 0, stg_count = 0;
+    for (;;) {
+      // every wait is followed by a vote so that all epilogue threads leave together
+      bool ok = wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true);
+      if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) break;
+      const int u = ctl->sunit[sslot];
+      ptx::mbar_arrive(&ctl->sempty[sslot]);
+      if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
+      if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
-      if (!wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true)) break;
+      ok = wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true);
+      if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      if (a.mode == MODE_LOGITS)
+      if (t.kind == U_LOGITS)
         epi_logits(a, s, t, tbase, r);
-      else if (a.mode == MODE_DX)
+      else if (t.kind == U_DX)
         epi_dx(a, s, t, tbase, r);
       else
-        epi_dw(a, t, tbase, r);
+        epi_dw(a, &maps, t, tbase, r, leader, stg, stg_count);
       ptx::tc_fence_before();
       ptx::mbar_arrive(&ctl->tempty[acc]);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (leader) ptx::bulk_wait_all();
   }
 
   __syncthreads();
@@ -395,9 +438,8 @@ cudaError_t gemm_prepare(int /*device*/) {
   return cudaFuncSetAttribute(flce_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
 }
 
-cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
-                        cudaStream_t st) {
-  flce_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, a);
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
+  flce_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(m, a);
   return cudaGetLastError();
 }
 

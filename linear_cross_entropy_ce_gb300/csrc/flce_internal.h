@@ -24,24 +24,24 @@ constexpr int BK = 64;
 
 enum GemmMode : int {
   MODE_LOGITS = 0,  // z = Xc W^T, epilogue: per-tile (max, sum exp), z_t, shifted bf16 logits
-  MODE_DX = 1,      // grad_hidden rows = dz W
-  MODE_DW = 2,      // grad_weight (+)= dz^T Xc
+  MODE_BWD = 1,     // one launch holding both consumers of dz:
+                    //   grad_hidden rows = dz W          (units [0, n_dx))
+                    //   grad_weight (+)= dz^T Xc         (units [n_dx, n_dx + n_dw))
 };
 
 struct GemmArgs {
   int mode;
   const int* hdr;       // workspace header (n_valid lives in HDR_NVALID)
   int* status;          // workspace header word HDR_STATUS
+  int* counter;         // dynamic tile counter of this launch (zero before it)
   long long c0;         // first compacted row of this chunk
   int C;                // chunk capacity (rows)
   int H, V;
   long long ldz;        // row stride (elements) of the chunk logits buffer
   int nvt;              // ceil(V / BN)
-  int splits;           // DX: number of vocabulary splits
-  int kb_per_split;     // DX: K blocks per split
   int store_z;          // LOGITS: write the shifted bf16 logits
-  int accumulate;       // DW: add into grad_weight (chunks after the first)
-  int first_chunk;      // DW: chunk 0 (writes zeros when it is empty)
+  int accumulate;       // BWD: add into grad_weight (chunks after the first)
+  int first_chunk;      // BWD: chunk 0 (writes zeros when it is empty)
   unsigned long long timeout_ns;
   // epilogue operands
   uint16_t* z;          // [C][ldz] bf16
@@ -50,18 +50,24 @@ struct GemmArgs {
   const int* tc;        // [C] chunk targets (-1 for padding rows)
   const int* idx;       // [N] compacted row -> token row
   uint16_t* grad_hidden;// [N][H] bf16
-  float* dxp;           // [splits][C][H] fp32 partials (splits > 1)
-  float* grad_weight;   // [V][H] fp32
+  float* grad_weight;   // [V][H] fp32 (zero fill of an empty first chunk)
+};
+
+// Tensor maps of one launch.  LOGITS: a0 = Xc (K-major), b0 = W (K-major).
+// BWD: a0 = dz (K-major), b0 = W (MN-major), a1 = dz (MN-major view),
+// b1 = Xc (MN-major), out = grad_weight (fp32, store / reduce-add).
+struct GemmMaps {
+  CUtensorMap a0, b0, a1, b1, out;
 };
 
 int gemm_smem_bytes();
 cudaError_t gemm_prepare(int device);
-cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& ta,
-                        const CUtensorMap& tb, int grid, cudaStream_t s);
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s);
 
 // Elementwise / bookkeeping kernels (flce_aux.cu).
 cudaError_t launch_prep(const int* targets, long long N, int V, int ignore_index,
-                        int* hdr, int* idx, int* n_valid_out, cudaStream_t s);
+                        int* hdr, int* idx, int* n_valid_out, int* counters, int n_counters,
+                        cudaStream_t s);
 cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, int H,
                                 uint16_t* grad_hidden, cudaStream_t s);
 cudaError_t launch_gather(const uint16_t* hidden, const int* targets, const int* hdr,
@@ -71,9 +77,6 @@ cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long 
                           int nvt, const float2* part, const float* zt, const int* tc,
                           float* rl, uint16_t* z, int reduce_sum, int make_dz,
                           cudaStream_t s);
-cudaError_t launch_dx_reduce(const int* hdr, const int* idx, long long c0, int C, int H,
-                             int splits, const float* dxp, uint16_t* grad_hidden,
-                             cudaStream_t s);
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl,
                             long long N, int reduce_sum, float* loss, int* n_valid_out,
                             float* row_loss, cudaStream_t s);

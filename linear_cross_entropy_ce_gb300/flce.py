@@ -34,7 +34,7 @@ class FlceError(RuntimeError):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("chunk_rows", ctypes.c_int64), ("max_chunks", ctypes.c_int64),
-                ("logits_row_stride", ctypes.c_int64), ("dx_splits", ctypes.c_int32),
+                ("logits_row_stride", ctypes.c_int64), ("gemm_launches_per_chunk", ctypes.c_int32),
                 ("vocab_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
 
 
@@ -210,7 +210,7 @@ def profile_end() -> dict:
     s = library().flce_profile_end(ms, n, ctypes.byref(total))
     if s != FLCE_OK:
         raise FlceError(s, "flce_profile_end")
-    names = ("logits", "grad_hidden", "grad_weight")
+    names = ("logits", "backward", "unused")
     return {"gemm_ms": dict(zip(names, list(ms))), "gemm_launches": dict(zip(names, list(n))),
             "kernel_launches": int(total.value)}
 
