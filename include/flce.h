@@ -153,6 +153,35 @@ flce_status flce_selftest_timeout(void* workspace, uint64_t timeout_ns,
                                   void* stream);
 
 /*
+ * flce_fwd_bwd without a workspace argument, for callers that cannot
+ * allocate device memory (code inside a CUDA graph capture or an allocator
+ * hook, plugins whose host framework owns every cudaMalloc, fixed memory
+ * budgets).  The pages have no counterpart: it is a deployment variant of
+ * flce_fwd_bwd with the same arguments, outputs and tolerances.
+ *   Scratch: a static device array of FLCE_NOALLOC_WORKSPACE_BYTES (64 MiB)
+ *     inside the library, held by every GPU that loads the library until the
+ *     process exits.  The call itself allocates nothing.
+ *   Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   Limits: sizes whose smallest plan (one 128-token chunk) does not fit in
+ *     the array are rejected with FLCE_EWORKSPACE; larger problems run with
+ *     smaller chunks than flce_fwd_bwd's default plan.
+ *   Sharing: every call on a device uses the same array.  Calls that overlap
+ *     on the GPU (other streams, other threads) race and give wrong results;
+ *     serialise them.  The array needs no clearing between calls.
+ *   Device-side status (bad targets, time-outs) is written into the array
+ *     and cannot be read back through flce_query_status.
+ */
+#define FLCE_NOALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+flce_status flce_fwd_bwd_noalloc(const void* hidden, const void* weight,
+                                 const int32_t* targets, int64_t N, int64_t H,
+                                 int64_t V, int32_t ignore_index, uint32_t flags,
+                                 float* loss, int32_t* n_valid, float* row_loss,
+                                 void* grad_hidden, float* grad_weight,
+                                 void* stream);
+
+/*
  * Launch profiling (for benchmarks).  Between flce_profile_begin() and
  * flce_profile_end(), every call records a pair of CUDA events around each
  * of its tcgen05 GEMM launches on the call's stream and counts every kernel

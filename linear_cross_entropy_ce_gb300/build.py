@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(OUT_DIR, "libflce.so")
-SOURCES = ["flce_gemm.cu", "flce_aux.cu", "flce_api.cu"]
+SOURCES = ["flce_gemm.cu", "flce_aux.cu", "flce_api.cu", "flce_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -313,6 +313,18 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
 
 }  // namespace
 
+namespace flce {
+// Forward+backward on a caller-provided device workspace (used by the entry
+// point whose scratch is a static device array).
+flce_status fwd_bwd_on_workspace(const void* hidden, const void* weight, const int32_t* targets, int64_t N,
+                                 int64_t H, int64_t V, int32_t ignore_index, uint32_t flags, float* loss,
+                                 int32_t* n_valid, float* row_loss, void* grad_hidden, float* grad_weight,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return run(hidden, weight, targets, N, H, V, ignore_index, flags, loss, n_valid, row_loss, grad_hidden,
+             grad_weight, workspace, workspace_bytes, stream, false);
+}
+}  // namespace flce
+
 extern "C" {
 
 size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags) {
