@@ -138,10 +138,14 @@ def cpu_cores():
 
 
 def cpu_baseline(p, target_s=12.0):
+    # grow the sample until it is about 10-30 s of CPU work
     rows = 16
     dt, n = oracle_sample_time(p, rows)
-    rows = int(max(16, min(4096, rows * target_s / max(dt, 1e-3))))
-    dt, n = oracle_sample_time(p, rows)
+    for _ in range(4):
+        if dt >= 10.0 or n < rows:
+            break
+        rows = int(max(rows + 16, min(8192, rows * target_s / max(dt, 1e-3))))
+        dt, n = oracle_sample_time(p, rows)
     w = p["workload"]
     return {"value": n / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": f"fp64 numpy oracle, full fwd+bwd of the first {n} valid tokens of {w.name} "
@@ -203,6 +207,7 @@ def main():
     import torch
     import torch.distributed as dist
     from linear_cross_entropy_ce_gb300 import flce, workloads as wl
+    from linear_cross_entropy_ce_gb300 import dist as fdist
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -217,7 +222,7 @@ def main():
     base = wl.WORKLOADS[args.workload]
     if args.tokens:
         base = base.with_shape(N=args.tokens)
-    w = base.with_shape(seed=base.seed + 1000 * rank) if rank else base
+    w = base.with_shape(seed=fdist.replica_seed(base.seed, rank))
     p = wl.make_inputs(w)
     N, H, V = w.N, w.H, w.V
     h = torch.from_numpy(p["hidden"].view(np.int16)).view(torch.bfloat16).to(dev)
@@ -259,11 +264,7 @@ def main():
         dist.barrier()
     prof = flce.profile_end()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        m = torch.tensor([ms], device=dev)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        ms = float(m.item())
+    ms = fdist.max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
 
     # end to end through the public API: pinned host inputs in, loss out, every step
     e2e = None
@@ -290,11 +291,7 @@ def main():
             e2e_step()
         a1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a0.elapsed_time(a1) / args.steps
-        if world > 1:
-            m = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(m, op=dist.ReduceOp.MAX)
-            e2e_ms = float(m.item())
+        e2e_ms = fdist.max_over_ranks(a0.elapsed_time(a1) / args.steps, dev)
         e2e = {"value": world * N / (e2e_ms / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": N * H * 2 + N * 4, "d2h_bytes_per_step": 8,
                "ms_per_step": e2e_ms, "note": "hidden and targets copied from pinned host memory each step, "
