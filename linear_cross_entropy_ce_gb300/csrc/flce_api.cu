@@ -12,6 +12,7 @@
 // The only buffer that scales with V is the C x V bf16 chunk of logits, so
 // the default plan keeps the workspace below 5% of the N x V bf16 logits.
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -46,6 +47,7 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int major = 0;
+  int pairs = 0;   // CTA pairs of the GEMM that fit on the device at once
 };
 
 constexpr int MAX_DEVICES = 64;
@@ -63,6 +65,8 @@ cudaError_t device_state(DeviceState* out) {
     if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
     if ((e = gemm_prepare(dev)) != cudaSuccess) return e;
+    if ((e = gemm_max_pairs(&d.pairs)) != cudaSuccess) return e;
+    if (d.pairs < 1) return cudaErrorInvalidConfiguration;
     d.ready = true;
   }
   *out = d;
@@ -83,23 +87,32 @@ unsigned long long wait_timeout_ns() {
 // ---------------------------------------------------------------------------
 struct Plan {
   long long N = 0, H = 0, V = 0, C = 0, ldz = 0, n_chunks = 0;
-  int nvt = 0, n_counters = 0;
+  int nvt = 0, splits = 1, kb_per_split = 0;
+  long long n_counters = 0, flags_per_chunk = 0;
   bool fwd_only = false;
-  size_t o_idx = 0, o_rl = 0, o_cnt = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, total = 0;
+  size_t o_idx = 0, o_rl = 0, o_cnt = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, o_dx = 0, total = 0;
 };
 
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
+constexpr int DEFAULT_PAIRS = 76;
+constexpr int MAX_SPLITS = 16;
+
 // Workspace layout for chunks of C rows.  Only the bf16 C x V logits buffer
 // (absent for the forward-only call) grows with V.
-Plan layout(long long N, long long H, long long V, long long C, bool fwd_only) {
+Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_only) {
   Plan p;
   p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only;
   p.ldz = cdiv(V, 64) * 64;
   p.nvt = static_cast<int>(cdiv(V, BN));
   p.n_chunks = cdiv(N, C);
-  p.n_counters = static_cast<int>(2 * p.n_chunks);   // one tile counter per GEMM launch
+  const long long kbt = cdiv(V, BK);
+  if (fwd_only) S = 1;
+  p.kb_per_split = static_cast<int>(cdiv(kbt, S));
+  p.splits = static_cast<int>(cdiv(kbt, p.kb_per_split));
+  p.flags_per_chunk = p.splits > 1 ? 2 * cdiv(C, PAIR_M) * cdiv(H, BN) : 0;
+  p.n_counters = p.n_chunks * (2 + p.flags_per_chunk);   // tile counters, then split flags
   size_t off = al256(HDR_WORDS * sizeof(int));
   p.o_idx = off;  off += al256(size_t(N) * 4);
   p.o_rl = off;   off += al256(size_t(N) * 4);
@@ -108,24 +121,53 @@ Plan layout(long long N, long long H, long long V, long long C, bool fwd_only) {
   p.o_tc = off;   off += al256(size_t(C) * 4);
   p.o_zt = off;   off += al256(size_t(C) * 4);
   p.o_part = off; off += al256(size_t(C) * p.nvt * 8);
-  if (!fwd_only) { p.o_z = off; off += al256(size_t(C) * p.ldz * 2); }
+  if (!fwd_only) {
+    p.o_z = off; off += al256(size_t(C) * p.ldz * 2);
+    if (p.splits > 1) { p.o_dx = off; off += al256(size_t(C) * H * 4); }
+  }
   p.total = off;
   return p;
 }
 
+// Vocabulary splits of the grad_hidden GEMM: with dynamic scheduling a dX
+// tile (K = V) should take at most half of a pair's average share of the
+// backward launch, or it alone sets the launch's length.
+int preferred_splits(long long C, long long H, long long V, int pairs) {
+  const double mt = double(cdiv(C, PAIR_M)), nt = double(cdiv(H, BN));
+  const double work = mt * nt * double(V) + double(cdiv(V, PAIR_M)) * nt * double(C);
+  const double per_pair = work / double(pairs);
+  long long S = static_cast<long long>(std::ceil(double(V) / (0.5 * per_pair)));
+  const long long max_by_k = std::max<long long>(1, cdiv(V, BK) / 8);   // >= 8 K blocks per split
+  S = std::min<long long>(std::min<long long>(S, MAX_SPLITS), max_by_k);
+  return static_cast<int>(std::max<long long>(S, 1));
+}
+
 long long max_chunk(long long N) { return cdiv(N, BM) * BM; }
 
+Plan plan_for_chunk(long long N, long long H, long long V, long long C, bool fwd_only, int pairs, size_t bytes) {
+  Plan p = layout(N, H, V, C, preferred_splits(C, H, V, pairs), fwd_only);
+  if (p.total > bytes) p = layout(N, H, V, C, 1, fwd_only);
+  return p;
+}
+
 // Largest chunk (multiple of 128 rows) whose plan fits in `bytes`.
-bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, Plan* out) {
+bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, int pairs, Plan* out) {
   long long lo = BM, hi = max_chunk(N);
-  if (layout(N, H, V, lo, fwd_only).total > bytes) return false;
+  if (layout(N, H, V, lo, 1, fwd_only).total > bytes) return false;
   while (lo < hi) {   // the size grows with C: bisect over multiples of 128
     const long long mid = ((lo / BM + hi / BM + 1) / 2) * BM;
-    if (layout(N, H, V, mid, fwd_only).total <= bytes) lo = mid;
+    if (layout(N, H, V, mid, 1, fwd_only).total <= bytes) lo = mid;
     else hi = mid - BM;
   }
-  *out = layout(N, H, V, lo, fwd_only);
+  *out = plan_for_chunk(N, H, V, lo, fwd_only, pairs, bytes);
   return true;
+}
+
+int device_pairs() {
+  DeviceState d;
+  if (device_state(&d) == cudaSuccess) return d.pairs;
+  cudaGetLastError();
+  return DEFAULT_PAIRS;
 }
 
 bool sizes_ok(long long N, long long H, long long V) {
@@ -135,9 +177,10 @@ bool sizes_ok(long long N, long long H, long long V) {
 size_t default_bytes(long long N, long long H, long long V, bool fwd_only) {
   if (!sizes_ok(N, H, V)) return 0;
   const size_t budget = size_t(N) * size_t(V) * 2 / 20;   // 5% of the bf16 logits
+  const int pairs = device_pairs();
   Plan p;
-  if (plan_for_bytes(N, H, V, fwd_only, budget, &p)) return p.total;
-  return layout(N, H, V, BM, fwd_only).total;             // never below one 128-row chunk
+  if (plan_for_bytes(N, H, V, fwd_only, budget, pairs, &p)) return p.total;
+  return plan_for_chunk(N, H, V, BM, fwd_only, pairs, ~size_t(0)).total;   // never below one 128-row chunk
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -233,7 +276,7 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   if (device_state(&dev) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
   if (dev.major < 10) return FLCE_EUNSUPPORTED;
   Plan p;
-  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, &p)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, dev.pairs, &p)) return FLCE_EWORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* hdr = at<int>(ws, 0);
@@ -245,17 +288,20 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   float* zt = at<float>(ws, p.o_zt);
   float2* part = at<float2>(ws, p.o_part);
   uint16_t* z = fwd_only ? nullptr : at<uint16_t>(ws, p.o_z);
+  float* dxacc = (!fwd_only && p.splits > 1) ? at<float>(ws, p.o_dx) : nullptr;
 
   GemmMaps fm, bm;   // forward (logits) and backward (dX + dW) launches
   std::memset(&fm, 0, sizeof(fm));
   std::memset(&bm, 0, sizeof(bm));
   const unsigned long long hb = static_cast<unsigned long long>(H) * 2;
-  bool ok = make_map(&fm.a0, xc, H, p.C, hb, BK, BM) && make_map(&fm.b0, weight, H, V, hb, BK, BN);
+  bool ok = make_map(&fm.a0, xc, H, p.C, hb, BK, BM) && make_map(&fm.b0, weight, H, V, hb, BK, BN / 2);
   if (!fwd_only)
     ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, weight, H, V, hb, 64, BK) &&
          make_map(&bm.a1, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&bm.b1, xc, H, p.C, hb, 64, BK) &&
          make_map(&bm.out, grad_weight, H, V, static_cast<unsigned long long>(H) * 4, 32, BM,
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32) &&
+         (!dxacc || make_map(&bm.dx, dxacc, H, p.C, static_cast<unsigned long long>(H) * 4, 32, BM,
+                             CU_TENSOR_MAP_DATA_TYPE_FLOAT32));
   if (!ok) return FLCE_ECUDA;
 
   const int reduce_sum = (flags & FLCE_REDUCE_SUM) ? 1 : 0;
@@ -277,10 +323,15 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   g.idx = idx;
   g.grad_hidden = static_cast<uint16_t*>(grad_hidden);
   g.grad_weight = grad_weight;
+  g.splits = p.splits;
+  g.kb_per_split = p.kb_per_split;
+  g.dxacc = dxacc;
 
-  const long long mt = cdiv(p.C, BM), ht = cdiv(H, BN);
-  const int grid_logits = static_cast<int>(std::min<long long>(mt * p.nvt, dev.sms));
-  const int grid_bwd = static_cast<int>(std::min<long long>(mt * ht + cdiv(V, BM) * ht, dev.sms));
+  // persistent grids: CTA pairs, no more than fit on the device at once
+  const long long mt = cdiv(p.C, PAIR_M), ht = cdiv(H, BN);
+  const int grid_logits = 2 * static_cast<int>(std::min<long long>(mt * p.nvt, dev.pairs));
+  const int grid_bwd =
+      2 * static_cast<int>(std::min<long long>(mt * ht * p.splits + cdiv(V, PAIR_M) * ht, dev.pairs));
 
   auto chk = [](cudaError_t e) { return e == cudaSuccess; };
   count_launches(2 + (fwd_only ? 0 : 1) + p.n_chunks * 2);   // prep, zero, finalize; gather + lse_dz per chunk
@@ -294,15 +345,17 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
     g.c0 = c0;
     if (!chk(launch_gather(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H, xc, tc, st)))
       return FLCE_ECUDA;
+    int* sync = counters + c * (2 + p.flags_per_chunk);
     g.mode = MODE_LOGITS;
-    g.counter = counters + 2 * c;
+    g.counter = sync;
     if (!chk(gemm_launch(g, fm, grid_logits, st))) return FLCE_ECUDA;
     if (!chk(launch_lse_dz(hdr, c0, g.C, g.V, p.ldz, p.nvt, part, zt, tc, rl, z, reduce_sum, fwd_only ? 0 : 1,
                            st)))
       return FLCE_ECUDA;
     if (fwd_only) continue;
     g.mode = MODE_BWD;
-    g.counter = counters + 2 * c + 1;
+    g.counter = sync + 1;
+    g.flags = sync + 2;
     g.accumulate = c > 0 ? 1 : 0;
     g.first_chunk = c == 0 ? 1 : 0;
     if (!chk(gemm_launch(g, bm, grid_bwd, st))) return FLCE_ECUDA;
@@ -341,7 +394,7 @@ size_t flce_workspace_bytes_for_chunk(int64_t N, int64_t H, int64_t V, uint32_t 
   if ((flags & ~FLCE_REDUCE_SUM) || !sizes_ok(N, H, V) || chunk_rows < 1) return 0;
   long long C = cdiv(chunk_rows, BM) * BM;
   if (C > max_chunk(N)) C = max_chunk(N);
-  return layout(N, H, V, C, false).total;
+  return plan_for_chunk(N, H, V, C, false, device_pairs(), ~size_t(0)).total;
 }
 
 flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags, int forward_only, size_t workspace_bytes,
@@ -350,11 +403,12 @@ flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags, int forwa
   if (N < 1 || H < 1 || V < 1) return FLCE_EINVAL;
   if (!sizes_ok(N, H, V)) return FLCE_EUNSUPPORTED;
   Plan p;
-  if (!plan_for_bytes(N, H, V, forward_only != 0, workspace_bytes, &p)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, forward_only != 0, workspace_bytes, device_pairs(), &p)) return FLCE_EWORKSPACE;
   out->chunk_rows = p.C;
   out->max_chunks = p.n_chunks;
   out->logits_row_stride = p.ldz;
   out->gemm_launches_per_chunk = forward_only ? 1 : 2;
+  out->dx_splits = p.splits;
   out->vocab_tiles = p.nvt;
   out->workspace_bytes = p.total;
   return FLCE_OK;

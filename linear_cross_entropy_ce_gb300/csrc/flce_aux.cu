@@ -66,7 +66,8 @@ constexpr int PREP_THREADS = 1024;
 
 __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restrict__ t, long long N, int V,
                                                              int ii, int* hdr, int* __restrict__ idx,
-                                                             int* n_valid_out, int* counters, int n_counters) {
+                                                             int* n_valid_out, int* counters,
+                                                             long long n_counters) {
   __shared__ int cnt[PREP_THREADS];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restric
     }
   }
   if (tid == 0) bad = 0;
-  for (int i = tid; i < n_counters; i += PREP_THREADS) counters[i] = 0;  // tile counters of the GEMMs
+  for (long long i = tid; i < n_counters; i += PREP_THREADS) counters[i] = 0;  // GEMM tile counters, split flags
   cnt[tid] = c;
   __syncthreads();
   if (mybad) bad = 1;
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restric
   if (tid == 0) {
     hdr[HDR_STATUS] = bad ? STATUS_BADTARGET : 0;
     hdr[HDR_NVALID] = total;
+    hdr[HDR_STALL] = 0;
     if (n_valid_out) *n_valid_out = total;
   }
 }
@@ -173,28 +175,40 @@ __global__ void __launch_bounds__(LSE_THREADS)
   const long long nv = hdr[HDR_NVALID];
   const float scale = reduce_sum ? 1.f : 1.f / static_cast<float>(nv);
   const int tgt = tc[r];
-  for (long long v0 = tid * 8LL; v0 < ldz; v0 += LSE_THREADS * 8LL) {
-    uint4 w = *reinterpret_cast<const uint4*>(zr + v0);
-    if (v0 >= V) {
-      *reinterpret_cast<uint4*>(zr + v0) = make_uint4(0u, 0u, 0u, 0u);
-      continue;
-    }
-    // the 8 columns lie in one 256-wide tile: z = stored + tile max
-    const float base = pr[v0 / BN].x - lse;
-    uint32_t in[4] = {w.x, w.y, w.z, w.w};
-    uint32_t out[4];
+  // four 8-column groups in flight per thread; each group lies in one
+  // 256-wide tile, where z = stored value + tile max
+  constexpr long long STEP = LSE_THREADS * 8LL;
+  for (long long v0 = tid * 8LL; v0 < ldz; v0 += 4 * STEP) {
+    uint4 w[4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const float s0 = __uint_as_float(in[g] << 16);
-      const float s1 = __uint_as_float(in[g] & 0xFFFF0000u);
-      const long long v = v0 + 2 * g;
-      float d0 = (exp2f((s0 + base) * LOG2E) - (v == tgt ? 1.f : 0.f)) * scale;
-      float d1 = (exp2f((s1 + base) * LOG2E) - (v + 1 == tgt ? 1.f : 0.f)) * scale;
-      if (v >= V) d0 = 0.f;
-      if (v + 1 >= V) d1 = 0.f;
-      out[g] = ptx::pack_bf16x2(d0, d1);
+    for (int q = 0; q < 4; ++q) {
+      const long long v = v0 + q * STEP;
+      w[q] = v < ldz ? *reinterpret_cast<const uint4*>(zr + v) : make_uint4(0u, 0u, 0u, 0u);
     }
-    *reinterpret_cast<uint4*>(zr + v0) = make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const long long v = v0 + q * STEP;
+      if (v >= ldz) break;
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (v < V) {
+        const float b2 = (pr[v / BN].x - lse) * LOG2E;
+        const uint32_t in[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+        uint32_t out[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float s0 = __uint_as_float(in[g] << 16);
+          const float s1 = __uint_as_float(in[g] & 0xFFFF0000u);
+          const long long c = v + 2 * g;
+          float d0 = (exp2f(fmaf(s0, LOG2E, b2)) - (c == tgt ? 1.f : 0.f)) * scale;
+          float d1 = (exp2f(fmaf(s1, LOG2E, b2)) - (c + 1 == tgt ? 1.f : 0.f)) * scale;
+          if (c >= V) d0 = 0.f;
+          if (c + 1 >= V) d1 = 0.f;
+          out[g] = ptx::pack_bf16x2(d0, d1);
+        }
+        o = make_uint4(out[0], out[1], out[2], out[3]);
+      }
+      *reinterpret_cast<uint4*>(zr + v) = o;
+    }
   }
 }
 
@@ -241,7 +255,7 @@ inline int grid_for(long long work, int threads, int cap) {
 }  // namespace
 
 cudaError_t launch_prep(const int* targets, long long N, int V, int ii, int* hdr, int* idx, int* n_valid_out,
-                        int* counters, int n_counters, cudaStream_t s) {
+                        int* counters, long long n_counters, cudaStream_t s) {
   prep_kernel<<<1, PREP_THREADS, 0, s>>>(targets, N, V, ii, hdr, idx, n_valid_out, counters, n_counters);
   return cudaGetLastError();
 }

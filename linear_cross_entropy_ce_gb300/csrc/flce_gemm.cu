@@ -10,47 +10,53 @@
 //                tricks"), the target logit, and z - m stored as bf16.
 //   MODE_BWD     the two consumers of dz in one launch:
 //     dX units   dX = dz W            A = dz [C,V] K-major,  B = W [V,H] MN-major
-//                epilogue: bf16 rows of grad_hidden, scattered to token rows.
+//                epilogue: bf16 rows of grad_hidden, scattered to token rows;
+//                with the vocabulary split in S parts, the parts are summed in
+//                fp32 in split order (TMA store, then reduce-adds, each part
+//                waiting for the previous one), and the last part converts.
 //     dW units   dW (+)= dz^T Xc      A = dz^T (MN-major view of dz), B = Xc MN-major
 //                epilogue: fp32 tile staged in shared memory and written by a
 //                TMA store (first chunk) or a TMA reduce-add (later chunks),
 //                so the fp32 accumulation happens in L2 in fixed chunk order.
 //
-// One CTA per SM, 192 threads: warp 0 claims tiles from a global counter
-// (dynamic scheduling, so the long grad_hidden tiles and the short
-// grad_weight tiles share the SMs) and issues TMA loads into a 4-stage shared
-// memory ring; warp 1 allocates TMEM and one lane issues tcgen05.mma
-// (128 x 256 x 16, bf16 -> fp32); warps 2-5 drain the two TMEM accumulators
-// (double buffered, 2 x 256 columns) so the epilogue of one tile overlaps the
-// main loop of the next.  Every wait is bounded: on time-out the CTA raises
-// an abort flag, lets copies in flight land, frees TMEM and returns, and the
-// status word in the workspace records STATUS_TIMEOUT.
+// Each tile is 256 x 256 and is computed by a CTA pair (a cluster of two CTAs
+// on two SMs) with tcgen05.mma.cta_group::2: each CTA stages its 128 rows of
+// A and its 128 columns of B (32 KB per K block) and holds 128 accumulator
+// rows in its TMEM.  Per CTA: warp 0 issues TMA loads into a 6-stage ring (in
+// CTA 0 it also claims tiles from a global counter and hands them to both
+// CTAs), warp 1 allocates TMEM and, in CTA 0, one lane issues the MMAs for
+// the pair, warps 2-5 drain two TMEM accumulators (double buffered, 2 x 256
+// columns) so an epilogue overlaps the next tile's main loop.  Every wait is
+// bounded: on time-out a CTA raises an abort flag, lets copies in flight
+// land, frees TMEM and returns, and the workspace status word records
+// STATUS_TIMEOUT.
 #include "flce_internal.h"
 #include "flce_ptx.cuh"
 
 namespace flce {
 namespace {
 
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;     // 16 KB
-constexpr int B_BYTES = BN * BK * 2;     // 32 KB
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 rows of A
+constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STG_BYTES = BM * 32 * 4;   // one 128 x 32 fp32 slice of a grad_weight tile
+constexpr int STG_BYTES = BM * 32 * 4;      // one 128 x 32 fp32 slice of an output tile
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr int SCHED_SLOTS = 4;
-constexpr uint32_t EPI_BAR = 1;          // named barrier of the epilogue warps
+constexpr uint32_t EPI_BAR = 1;             // named barrier of the epilogue warps
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr int MN_BLOCK_BYTES = 64 * 128; // 64 K rows x 128 B (64 bf16 along M or N)
+constexpr int MN_BLOCK_BYTES = 64 * 128;    // 64 K rows x 128 B (64 bf16 along M or N)
+constexpr uint16_t PAIR_MASK = 0x3;
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t sfull[SCHED_SLOTS];
-  uint64_t sempty[SCHED_SLOTS];
+  uint64_t full[STAGES];       // CTA 0: both CTAs' loads of a stage landed
+  uint64_t empty[STAGES];      // each CTA: the pair's MMAs released the stage
+  uint64_t tfull[2];           // each CTA: accumulator ready
+  uint64_t tempty[2];          // CTA 0: both CTAs' epilogues drained the accumulator
+  uint64_t sfull[SCHED_SLOTS]; // each CTA: a tile id is in sunit
+  uint64_t sempty[SCHED_SLOTS];// CTA 0: every reader of the slot is done
   uint64_t mma_done;
   int sunit[SCHED_SLOTS];
   uint32_t tmem_base;
@@ -61,31 +67,65 @@ constexpr int CTL_BYTES = ((sizeof(Ctl) + 255) / 256) * 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STG_BYTES + CTL_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
+// Readers of a scheduler slot: in CTA 0 the MMA lane and its epilogue
+// threads, in CTA 1 the TMA lane and its epilogue threads.
+constexpr uint32_t SCHED_READERS = 2 * (1 + EPI_THREADS);
+
 // Bounded wait on an mbarrier phase.  Gives up (returning false) when the
 // CTA's abort flag is raised by another role, or after timeout_ns, in which
 // case it raises the flag itself.
+// Wait sites, recorded in the workspace header when a wait times out.
+enum WaitSite : int {
+  W_SCHED_EMPTY = 1, W_SCHED_FULL_PRODUCER = 2, W_STAGE_EMPTY = 3, W_DRAIN = 4, W_SCHED_FULL_MMA = 5,
+  W_TMEM_EMPTY = 6, W_STAGE_FULL = 7, W_MMA_DONE = 8, W_SCHED_FULL_EPI = 9, W_TMEM_FULL = 10, W_SPLIT_FLAG = 11
+};
+
+__device__ void record_stall(int* hdr, int site) {
+  const int code = site | (static_cast<int>(ptx::cluster_ctarank()) << 8) | (static_cast<int>(blockIdx.x) << 12);
+  atomicCAS(hdr + HDR_STALL, 0, code);
+}
+
 __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Ctl* ctl, uint64_t timeout_ns,
-                                        bool honor_abort) {
-  if (ptx::mbar_test(bar, parity)) return true;
+                                        bool honor_abort, int* hdr, int site) {
+  if (ptx::mbar_test_cluster(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_test(bar, parity)) return true;
+    if (ptx::mbar_test_cluster(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (honor_abort && *reinterpret_cast<volatile int*>(&ctl->abort)) return false;
       if (ptx::global_timer_ns() - t0 > timeout_ns) {
         *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+        record_stall(hdr, site);
         return false;
       }
     }
   }
 }
 
+// Bounded wait until a global flag reaches `target`.
+__device__ __noinline__ bool wait_flag(const int* flag, int target, Ctl* ctl, uint64_t timeout_ns, int* hdr) {
+  if (ptx::ld_acquire_gpu(flag) >= target) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::ld_acquire_gpu(flag) >= target) return true;
+    if ((i & 15u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+      if (ptx::global_timer_ns() - t0 > timeout_ns) {
+        *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+        record_stall(hdr, W_SPLIT_FLAG);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
 struct Shape {
   int Cl;         // valid rows in this chunk
-  int mt, nt;     // LOGITS: tiles along M and N; BWD: dX tiles along M and N
+  int mt, nt;     // LOGITS: pair tiles along M and N; BWD: dX pair tiles along M and N
   int kbt;        // LOGITS: K blocks
   int n_dx;       // BWD: number of dX units (they come first)
-  int dw_mt;      // BWD: dW tiles along M (vocabulary)
+  int dw_mt;      // BWD: dW pair tiles along M (vocabulary)
   int units;
 };
 
@@ -94,7 +134,7 @@ __device__ __forceinline__ Shape make_shape(const GemmArgs& a) {
   const long long nv = a.hdr[HDR_NVALID];
   const long long rem = nv - a.c0;
   s.Cl = rem <= 0 ? 0 : (rem >= a.C ? a.C : static_cast<int>(rem));
-  s.mt = (s.Cl + BM - 1) / BM;
+  s.mt = (s.Cl + PAIR_M - 1) / PAIR_M;
   if (a.mode == MODE_LOGITS) {
     s.nt = a.nvt;
     s.kbt = (a.H + BK - 1) / BK;
@@ -104,8 +144,8 @@ __device__ __forceinline__ Shape make_shape(const GemmArgs& a) {
   } else {
     s.nt = (a.H + BN - 1) / BN;
     s.kbt = 0;
-    s.n_dx = s.mt * s.nt;
-    s.dw_mt = (a.V + BM - 1) / BM;
+    s.n_dx = s.mt * s.nt * a.splits;
+    s.dw_mt = (a.V + PAIR_M - 1) / PAIR_M;
     s.units = s.Cl > 0 ? s.n_dx + s.dw_mt * s.nt : 0;
   }
   return s;
@@ -114,34 +154,45 @@ __device__ __forceinline__ Shape make_shape(const GemmArgs& a) {
 enum UnitKind : int { U_LOGITS = 0, U_DX = 1, U_DW = 2 };
 
 struct Unit {
-  int kind, m0, n0, ntile, kb1;
+  int kind;
+  int m0, n0;     // pair tile origin (rows of the pair, columns)
+  int ntile;      // vocab tile (LOGITS), dX tile index (DX)
+  int split;      // DX vocabulary split
+  int kb0, kb1;
 };
 
-// Tile order: LOGITS walks M fastest so the CTAs in flight share one W tile;
-// dX and dW walk N fastest so they share one slab of dz.
+// Tile order: LOGITS walks M fastest so the pairs in flight share one W tile;
+// dX and dW walk N fastest so they share one slab of dz.  dX splits come in
+// increasing split order, so every split is claimed after the previous one.
 __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const Shape& s, int u) {
   Unit t;
+  t.split = 0;
   if (a.mode == MODE_LOGITS) {
     const int m = u % s.mt, n = u / s.mt;
-    t.kind = U_LOGITS; t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.kb1 = s.kbt;
+    t.kind = U_LOGITS; t.m0 = m * PAIR_M; t.n0 = n * BN; t.ntile = n; t.kb0 = 0; t.kb1 = s.kbt;
   } else if (u < s.n_dx) {
-    const int n = u % s.nt, m = u / s.nt;
-    t.kind = U_DX; t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.kb1 = (a.V + BK - 1) / BK;
+    const int n = u % s.nt, rest = u / s.nt;
+    const int m = rest % s.mt, sp = rest / s.mt;
+    const int kbt = (a.V + BK - 1) / BK;
+    t.kind = U_DX; t.m0 = m * PAIR_M; t.n0 = n * BN; t.ntile = m * s.nt + n; t.split = sp;
+    t.kb0 = sp * a.kb_per_split;
+    t.kb1 = min(kbt, t.kb0 + a.kb_per_split);
   } else {
     const int w = u - s.n_dx;
     const int n = w % s.nt, m = w / s.nt;
-    t.kind = U_DW; t.m0 = m * BM; t.n0 = n * BN; t.ntile = n; t.kb1 = (s.Cl + BK - 1) / BK;
+    t.kind = U_DW; t.m0 = m * PAIR_M; t.n0 = n * BN; t.ntile = n; t.kb0 = 0; t.kb1 = (s.Cl + BK - 1) / BK;
   }
   return t;
 }
 
 // ---------------------------------------------------------------------------
-// epilogues (one thread = one accumulator row; tbase = this warp's lanes)
+// epilogues (one thread = one accumulator row of this CTA; tbase = this warp's
+// TMEM lanes; row0 = first row of this CTA's half of the pair tile)
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, const Unit& t, uint32_t tbase,
-                                           int r) {
-  const int grow = t.m0 + r;
+__device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, const Unit& t, int row0,
+                                           uint32_t tbase, int r) {
+  const int grow = row0 + r;
   const bool rv = grow < s.Cl;
   const int tgt = rv ? a.tc[grow] : -1;
   const int tl = tgt - t.n0;
@@ -186,8 +237,21 @@ __device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, co
   }
 }
 
-__device__ __forceinline__ void epi_dx(const GemmArgs& a, const Shape& s, const Unit& t, uint32_t tbase, int r) {
-  const int grow = t.m0 + r;
+__device__ __forceinline__ void store_bf16_row(uint16_t* dst, const float* v, int h, int H) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (h + g * 8 < H) {
+      const float* q = v + 8 * g;
+      *reinterpret_cast<uint4*>(dst + 8 * g) =
+          make_uint4(ptx::pack_bf16x2(q[0], q[1]), ptx::pack_bf16x2(q[2], q[3]), ptx::pack_bf16x2(q[4], q[5]),
+                     ptx::pack_bf16x2(q[6], q[7]));
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s, const Unit& t, int row0,
+                                              uint32_t tbase, int r) {
+  const int grow = row0 + r;
   const bool rv = grow < s.Cl;
   const long long tok = rv ? a.idx[a.c0 + grow] : 0;
 #pragma unroll 1
@@ -196,30 +260,21 @@ __device__ __forceinline__ void epi_dx(const GemmArgs& a, const Shape& s, const 
     if (h >= a.H) break;  // warp-uniform
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
-    if (!rv) continue;
-    uint16_t* dst = a.grad_hidden + tok * a.H + h;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      if (h + g * 8 < a.H) {
-        const float* q = v + 8 * g;
-        *reinterpret_cast<uint4*>(dst + 8 * g) =
-            make_uint4(ptx::pack_bf16x2(q[0], q[1]), ptx::pack_bf16x2(q[2], q[3]), ptx::pack_bf16x2(q[4], q[5]),
-                       ptx::pack_bf16x2(q[6], q[7]));
-      }
-    }
+    if (rv) store_bf16_row(a.grad_hidden + tok * a.H + h, v, h, a.H);
   }
 }
 
-// grad_weight tile: 32-column slices go TMEM -> registers -> shared memory
-// (128-byte swizzled rows, conflict-free) -> TMA store or reduce-add.  Two
-// staging buffers alternate; `leader` owns the bulk-group bookkeeping.
-__device__ __forceinline__ void epi_dw(const GemmArgs& a, const GemmMaps* maps, const Unit& t, uint32_t tbase,
-                                       int r, bool leader, uint8_t* stg, uint32_t& stg_count) {
-  (void)maps;
+// One 128 x 256 fp32 accumulator half -> 32-column slices -> shared memory
+// (128-byte swizzled rows, conflict-free) -> TMA store (reduce == false) or
+// TMA reduce-add into `map` at (n0 + 32 j, row0).  Two staging buffers
+// alternate; `leader` owns the bulk-group bookkeeping.
+__device__ __forceinline__ void tile_to_global(const CUtensorMap* map, int ncols_total, int n0, int row0,
+                                               bool reduce, uint32_t tbase, int r, bool leader, uint8_t* stg,
+                                               uint32_t& stg_count) {
 #pragma unroll 1
   for (int j = 0; j < BN / 32; ++j) {
-    const int h = t.n0 + j * 32;
-    if (h >= a.H) break;  // uniform over the epilogue warps
+    const int h = n0 + j * 32;
+    if (h >= ncols_total) break;  // uniform over the epilogue warps
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
     uint8_t* buf = stg + (stg_count & 1u) * STG_BYTES;
@@ -233,27 +288,75 @@ __device__ __forceinline__ void epi_dw(const GemmArgs& a, const GemmMaps* maps, 
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(EPI_BAR, EPI_THREADS);
     if (leader) {
-      if (a.accumulate)
-        ptx::tma_reduce_add_2d(&maps->out, buf, h, t.m0);
+      if (reduce)
+        ptx::tma_reduce_add_2d(map, buf, h, row0);
       else
-        ptx::tma_store_2d(&maps->out, buf, h, t.m0);
+        ptx::tma_store_2d(map, buf, h, row0);
       ptx::bulk_commit();
     }
     ++stg_count;
   }
 }
 
+// dX unit of a split vocabulary: split 0 stores its fp32 part, split k waits
+// until split k-1 has landed and reduce-adds onto it, the last split turns
+// the finished fp32 rows into bf16 grad_hidden rows.  Returns false on abort.
+__device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* maps, const Shape& s,
+                                             const Unit& t, int row0, uint32_t rank, uint32_t tbase, int r,
+                                             bool leader, uint8_t* stg, uint32_t& stg_count, Ctl* ctl) {
+  int* flag = a.flags + 2 * t.ntile + rank;
+  bool ok = true;
+  if (leader && t.split > 0) {
+    ok = wait_flag(flag, t.split, ctl, a.timeout_ns, const_cast<int*>(a.hdr));
+    ptx::fence_proxy_async_global();
+  }
+  if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) return false;
+  tile_to_global(&maps->dx, a.H, t.n0, row0, t.split > 0, tbase, r, leader, stg, stg_count);
+  if (leader) {
+    ptx::bulk_wait_all();                 // this part has landed in global memory
+    ptx::fence_proxy_async_global();
+    __threadfence();
+    ptx::st_release_gpu(flag, t.split + 1);
+  }
+  if (t.split == a.splits - 1) {
+    ptx::named_bar_sync(EPI_BAR, EPI_THREADS);
+    const int grow = row0 + r;
+    if (grow < s.Cl) {
+      const long long tok = a.idx[a.c0 + grow];
+      const float* src = a.dxacc + static_cast<size_t>(grow) * a.H;
+      for (int j = 0; j < BN / 32; ++j) {
+        const int h = t.n0 + j * 32;
+        if (h >= a.H) break;
+        float v[32];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          if (h + 4 * g < a.H) {
+            const float4 q = __ldcg(reinterpret_cast<const float4*>(src + h + 4 * g));
+            v[4 * g] = q.x; v[4 * g + 1] = q.y; v[4 * g + 2] = q.z; v[4 * g + 3] = q.w;
+          } else {
+            v[4 * g] = v[4 * g + 1] = v[4 * g + 2] = v[4 * g + 3] = 0.f;
+          }
+        }
+        store_bf16_row(a.grad_hidden + tok * a.H + h, v, h, a.H);
+      }
+    }
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     flce_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg = smem + STAGES * STAGE_BYTES;
   Ctl* ctl = reinterpret_cast<Ctl*>(stg + 2 * STG_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool lead = rank == 0;
 
-  const Shape s = make_shape(a);
+  const Shape s = make_shape(a);   // identical in both CTAs of a pair
   if (a.mode == MODE_BWD && s.Cl == 0) {
     // Empty first chunk (no valid token at all): grad_weight is zero.
     if (a.first_chunk) {
@@ -274,11 +377,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ctl->tfull[i], 1);
-      ptx::mbar_init(&ctl->tempty[i], EPI_THREADS);
+      ptx::mbar_init(&ctl->tempty[i], 2 * EPI_THREADS);
     }
     for (int i = 0; i < SCHED_SLOTS; ++i) {
       ptx::mbar_init(&ctl->sfull[i], 1);
-      ptx::mbar_init(&ctl->sempty[i], 1 + EPI_THREADS);
+      ptx::mbar_init(&ctl->sempty[i], SCHED_READERS);
     }
     ptx::mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
@@ -289,54 +392,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tma_prefetch_desc(&maps.a1);
       ptx::tma_prefetch_desc(&maps.b1);
       ptx::tma_prefetch_desc(&maps.out);
+      if (a.splits > 1) ptx::tma_prefetch_desc(&maps.dx);
     }
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, TMEM_COLS);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(&ctl->tmem_base, TMEM_COLS);   // collective over the pair
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();   // both CTAs' barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const uint64_t to = a.timeout_ns;
+  int* hdr = const_cast<int*>(a.hdr);
+  const int half = static_cast<int>(rank) * BM;   // this CTA's rows (A) / columns (B) inside a pair tile
 
   if (warp == 0 && lane == 0) {
-    // ---------------- scheduler + TMA producer ----------------
+    // ---------------- (CTA 0: scheduler +) TMA producer ----------------
     uint32_t stage = 0, phase = 0, sslot = 0, sphase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
     for (;;) {
-      if (!wait_phase(&ctl->sempty[sslot], sphase ^ 1u, ctl, to, true)) { ok = false; break; }
-      int u = atomicAdd(a.counter, 1);
-      if (u >= s.units) u = -1;
-      ctl->sunit[sslot] = u;
-      ptx::mbar_arrive(&ctl->sfull[sslot]);
+      int u;
+      if (lead) {
+        if (!wait_phase(&ctl->sempty[sslot], sphase ^ 1u, ctl, to, true, hdr, W_SCHED_EMPTY)) { ok = false; break; }
+        u = atomicAdd(a.counter, 1);
+        if (u >= s.units) u = -1;
+        ctl->sunit[sslot] = u;
+        ptx::st_remote_u32(ptx::map_to_rank(&ctl->sunit[sslot], 1), static_cast<uint32_t>(u));
+        ptx::mbar_arrive(&ctl->sfull[sslot]);
+        ptx::mbar_arrive_remote(ptx::map_to_rank(&ctl->sfull[sslot], 1));
+      } else {
+        if (!wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_PRODUCER)) { ok = false; break; }
+        u = ctl->sunit[sslot];
+        ptx::mbar_arrive_remote(ptx::map_to_rank(&ctl->sempty[sslot], 0));
+      }
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
-      for (int kb = 0; kb < t.kb1; ++kb) {
-        if (!wait_phase(&ctl->empty[stage], phase ^ 1u, ctl, to, true)) { ok = false; break; }
+      for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        if (!wait_phase(&ctl->empty[stage], phase ^ 1u, ctl, to, true, hdr, W_STAGE_EMPTY)) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
-        uint64_t* fb = &ctl->full[stage];
-        ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        const uint32_t fb = ptx::map_to_rank(&ctl->full[stage], 0);   // CTA 0's barrier
+        if (lead) ptx::mbar_arrive_expect_tx(&ctl->full[stage], 2 * STAGE_BYTES);
         const int k0 = kb * BK;
         if (t.kind == U_LOGITS) {
-          ptx::tma_load_2d(sa, &maps.a0, fb, k0, t.m0);      // Xc rows m0.., cols k0..
-          ptx::tma_load_2d(sb, &maps.b0, fb, k0, t.n0);      // W rows n0.., cols k0..
+          ptx::tma_load_2d_pair(sa, &maps.a0, fb, k0, t.m0 + half);      // Xc rows, cols k0..
+          ptx::tma_load_2d_pair(sb, &maps.b0, fb, k0, t.n0 + half);      // W rows (vocab), cols k0..
         } else if (t.kind == U_DX) {
-          ptx::tma_load_2d(sa, &maps.a0, fb, k0, t.m0);      // dz rows m0.., vocab k0..
+          ptx::tma_load_2d_pair(sa, &maps.a0, fb, k0, t.m0 + half);      // dz rows, vocab k0..
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)                    // W rows k0.., cols n0+64j..
-            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &maps.b0, fb, t.n0 + 64 * j, k0);
+          for (int j = 0; j < BN / 128; ++j)                              // W rows k0.., cols n0+half+64j
+            ptx::tma_load_2d_pair(sb + j * MN_BLOCK_BYTES, &maps.b0, fb, t.n0 + half + 64 * j, k0);
         } else {
 #pragma unroll
-          for (int j = 0; j < BM / 64; ++j)                    // dz rows k0.., vocab m0+64j..
-            ptx::tma_load_2d(sa + j * MN_BLOCK_BYTES, &maps.a1, fb, t.m0 + 64 * j, k0);
+          for (int j = 0; j < BM / 64; ++j)                               // dz rows k0.., vocab m0+half+64j
+            ptx::tma_load_2d_pair(sa + j * MN_BLOCK_BYTES, &maps.a1, fb, t.m0 + half + 64 * j, k0);
 #pragma unroll
-          for (int j = 0; j < BN / 64; ++j)                    // Xc rows k0.., cols n0+64j..
-            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &maps.b1, fb, t.n0 + 64 * j, k0);
+          for (int j = 0; j < BN / 128; ++j)                              // Xc rows k0.., cols n0+half+64j
+            ptx::tma_load_2d_pair(sb + j * MN_BLOCK_BYTES, &maps.b1, fb, t.n0 + half + 64 * j, k0);
         }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -344,16 +460,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) break;
     }
-    if (!ok) {
-      // let the copies already in flight land before the CTA exits
+    if (!ok && lead) {
+      // let the copies already in flight land before the pair exits
       for (int i = 0; i < STAGES; ++i)
-        if (issued_mask & (1u << i)) wait_phase(&ctl->full[i], (issued_parity >> i) & 1u, ctl, to, false);
+        if (issued_mask & (1u << i)) wait_phase(&ctl->full[i], (issued_parity >> i) & 1u, ctl, to, false, hdr, W_DRAIN);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 && lane == 0 && lead) {
+    // ---------------- MMA issuer for the pair ----------------
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, sslot = 0, sphase = 0;
     for (;;) {
-      if (!wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true)) break;
+      if (!wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_MMA)) break;
       const int u = ctl->sunit[sslot];
       ptx::mbar_arrive(&ctl->sempty[sslot]);
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
@@ -361,15 +477,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Unit t = decode_unit(a, s, u);
       const int a_mn = t.kind == U_DW ? 1 : 0;
       const int b_mn = t.kind == U_LOGITS ? 0 : 1;
-      const uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, a_mn, b_mn);
+      const uint32_t idesc = ptx::idesc_bf16_f32(PAIR_M, BN, a_mn, b_mn);
       const uint32_t a_lbo = a_mn ? MN_BLOCK_BYTES : 16, b_lbo = b_mn ? MN_BLOCK_BYTES : 16;
       const uint32_t a_kstep = a_mn ? 16 * 128 : 32, b_kstep = b_mn ? 16 * 128 : 32;
-      if (!wait_phase(&ctl->tempty[acc], acc_phase ^ 1u, ctl, to, true)) break;
+      if (!wait_phase(&ctl->tempty[acc], acc_phase ^ 1u, ctl, to, true, hdr, W_TMEM_EMPTY)) break;
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem + acc * BN;
       bool ok = true;
-      for (int kb = 0; kb < t.kb1; ++kb) {
-        if (!wait_phase(&ctl->full[stage], phase, ctl, to, true)) { ok = false; break; }
+      for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        if (!wait_phase(&ctl->full[stage], phase, ctl, to, true, hdr, W_STAGE_FULL)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t sb = sa + A_BYTES;
@@ -377,55 +493,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint64_t ad = ptx::smem_desc_sw128(sa + kk * a_kstep, a_lbo, 1024);
           const uint64_t bd = ptx::smem_desc_sw128(sb + kk * b_kstep, b_lbo, 1024);
-          ptx::umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          ptx::umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
         }
-        ptx::umma_commit(&ctl->empty[stage]);   // frees the smem slot when these MMAs finish
+        ptx::umma_commit_pair(&ctl->empty[stage], PAIR_MASK);   // frees the slot in both CTAs
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      ptx::umma_commit(&ctl->tfull[acc]);       // accumulator ready for the epilogue
+      ptx::umma_commit_pair(&ctl->tfull[acc], PAIR_MASK);       // accumulator ready in both CTAs
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
-    ptx::umma_commit(&ctl->mma_done);
-    wait_phase(&ctl->mma_done, 0, ctl, to, false);
+    ptx::umma_commit_pair(&ctl->mma_done, 0x1);
+    wait_phase(&ctl->mma_done, 0, ctl, to, false, hdr, W_MMA_DONE);
   } else if (warp >= 2) {
-    // ---------------- epilogue ----------------
+    // ---------------- epilogue (both CTAs: 128 rows each) ----------------
     const int q = warp & 3;             // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;        // accumulator row
+    const int r = q * 32 + lane;        // accumulator row within this CTA's half
     const bool leader = warp == 2 && lane == 0;
+    const uint32_t sempty0 = ptx::map_to_rank(&ctl->sempty[0], 0);
+    const uint32_t tempty0 = ptx::map_to_rank(&ctl->tempty[0], 0);
     uint32_t acc = 0, acc_phase = 0, sslot = 0, sphase = 0, stg_count = 0;
     for (;;) {
       // every wait is followed by a vote so that all epilogue threads leave together
-      bool ok = wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true);
+      bool ok = wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_EPI);
       if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) break;
       const int u = ctl->sunit[sslot];
-      ptx::mbar_arrive(&ctl->sempty[sslot]);
+      ptx::mbar_arrive_remote(sempty0 + sslot * 8u);
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
-      ok = wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true);
+      ok = wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true, hdr, W_TMEM_FULL);
       if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int row0 = t.m0 + half;
+      bool cont = true;
       if (t.kind == U_LOGITS)
-        epi_logits(a, s, t, tbase, r);
+        epi_logits(a, s, t, row0, tbase, r);
+      else if (t.kind == U_DX && a.splits == 1)
+        epi_dx_direct(a, s, t, row0, tbase, r);
       else if (t.kind == U_DX)
-        epi_dx(a, s, t, tbase, r);
+        cont = epi_dx_split(a, &maps, s, t, row0, rank, tbase, r, leader, stg, stg_count, ctl);
       else
-        epi_dw(a, &maps, t, tbase, r, leader, stg, stg_count);
+        tile_to_global(&maps.out, a.H, t.n0, row0, a.accumulate != 0, tbase, r, leader, stg, stg_count);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&ctl->tempty[acc]);
+      ptx::mbar_arrive_remote(tempty0 + acc * 8u);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
+      if (!cont) break;
     }
     if (leader) ptx::bulk_wait_all();
   }
 
   __syncthreads();
+  ptx::cluster_sync();   // the peer no longer touches this CTA's barriers or TMEM
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, TMEM_COLS);
+    ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
   }
   if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) atomicOr(a.status, STATUS_TIMEOUT);
 }
@@ -438,7 +562,23 @@ cudaError_t gemm_prepare(int /*device*/) {
   return cudaFuncSetAttribute(flce_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
 }
 
+cudaError_t gemm_max_pairs(int* pairs) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(pairs, flce_gemm_kernel, &cfg);
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
+  // grid counts CTAs and must be even (pairs)
   flce_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(m, a);
   return cudaGetLastError();
 }

@@ -14,11 +14,14 @@ constexpr int STATUS_TIMEOUT = 2;
 // Workspace header words.
 constexpr int HDR_STATUS = 0;
 constexpr int HDR_NVALID = 1;
+constexpr int HDR_STALL = 2;   // first pipeline wait that timed out: site | rank << 8 | block << 12
 constexpr int HDR_WORDS = 64;
 
-// GEMM tile shape: one CTA owns a 128 x 256 fp32 accumulator in TMEM and
-// streams K in blocks of 64 bf16 (one 128-byte swizzle row).
+// GEMM tile shape: a CTA pair (cluster of 2, tcgen05 cta_group::2) owns a
+// 256 x 256 fp32 accumulator, 128 rows in each CTA's TMEM, and streams K in
+// blocks of 64 bf16 (one 128-byte swizzle row).  BM is the rows per CTA.
 constexpr int BM = 128;
+constexpr int PAIR_M = 2 * BM;
 constexpr int BN = 256;
 constexpr int BK = 64;
 
@@ -42,6 +45,9 @@ struct GemmArgs {
   int store_z;          // LOGITS: write the shifted bf16 logits
   int accumulate;       // BWD: add into grad_weight (chunks after the first)
   int first_chunk;      // BWD: chunk 0 (writes zeros when it is empty)
+  int splits;           // BWD: vocabulary splits of the grad_hidden GEMM
+  int kb_per_split;     // BWD: K blocks per split
+  int* flags;           // BWD, splits > 1: per (tile, CTA) count of finished splits (zero before)
   unsigned long long timeout_ns;
   // epilogue operands
   uint16_t* z;          // [C][ldz] bf16
@@ -51,22 +57,25 @@ struct GemmArgs {
   const int* idx;       // [N] compacted row -> token row
   uint16_t* grad_hidden;// [N][H] bf16
   float* grad_weight;   // [V][H] fp32 (zero fill of an empty first chunk)
+  const float* dxacc;   // [C][H] fp32 sum of the grad_hidden splits (splits > 1)
 };
 
 // Tensor maps of one launch.  LOGITS: a0 = Xc (K-major), b0 = W (K-major).
 // BWD: a0 = dz (K-major), b0 = W (MN-major), a1 = dz (MN-major view),
-// b1 = Xc (MN-major), out = grad_weight (fp32, store / reduce-add).
+// b1 = Xc (MN-major), out = grad_weight (fp32, store / reduce-add),
+// dx = the fp32 grad_hidden split accumulator (store / reduce-add).
 struct GemmMaps {
-  CUtensorMap a0, b0, a1, b1, out;
+  CUtensorMap a0, b0, a1, b1, out, dx;
 };
 
 int gemm_smem_bytes();
 cudaError_t gemm_prepare(int device);
+cudaError_t gemm_max_pairs(int* pairs);   // CTA pairs resident at once (current device)
 cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t s);
 
 // Elementwise / bookkeeping kernels (flce_aux.cu).
 cudaError_t launch_prep(const int* targets, long long N, int V, int ignore_index,
-                        int* hdr, int* idx, int* n_valid_out, int* counters, int n_counters,
+                        int* hdr, int* idx, int* n_valid_out, int* counters, long long n_counters,
                         cudaStream_t s);
 cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, int H,
                                 uint16_t* grad_hidden, cudaStream_t s);

@@ -35,6 +35,7 @@ class FlceError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("chunk_rows", ctypes.c_int64), ("max_chunks", ctypes.c_int64),
                 ("logits_row_stride", ctypes.c_int64), ("gemm_launches_per_chunk", ctypes.c_int32),
+                ("dx_splits", ctypes.c_int32),
                 ("vocab_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
 
 
