@@ -77,7 +77,7 @@ typedef struct flce_plan_info {
   int64_t logits_row_stride;/* elements per row of the bf16 chunk logits buffer*/
   int32_t gemm_launches_per_chunk; /* 2 (logits; grad_hidden + grad_weight), 1 fwd */
   int32_t dx_splits;        /* vocabulary splits of the grad_hidden GEMM        */
-  int32_t vocab_tiles;      /* ceil(V / 256)                                   */
+  int32_t vocab_tiles;      /* ceil(V / 256): logits tiles per 256 tokens      */
   size_t workspace_bytes;   /* bytes the plan uses (<= the bytes offered)      */
 } flce_plan_info;
 

@@ -87,7 +87,7 @@ unsigned long long wait_timeout_ns() {
 // ---------------------------------------------------------------------------
 struct Plan {
   long long N = 0, H = 0, V = 0, C = 0, ldz = 0, n_chunks = 0;
-  int nvt = 0, splits = 1, kb_per_split = 0;
+  int nvt = 0, nparts = 0, splits = 1, kb_per_split = 0;
   long long n_counters = 0, flags_per_chunk = 0;
   bool fwd_only = false;
   size_t o_idx = 0, o_rl = 0, o_cnt = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, o_dx = 0, total = 0;
@@ -106,12 +106,13 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
   p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only;
   p.ldz = cdiv(V, 64) * 64;
   p.nvt = static_cast<int>(cdiv(V, BN));
+  p.nparts = static_cast<int>(cdiv(V, PART_COLS));
   p.n_chunks = cdiv(N, C);
   const long long kbt = cdiv(V, BK);
   if (fwd_only) S = 1;
   p.kb_per_split = static_cast<int>(cdiv(kbt, S));
   p.splits = static_cast<int>(cdiv(kbt, p.kb_per_split));
-  p.flags_per_chunk = p.splits > 1 ? 2 * cdiv(C, PAIR_M) * cdiv(H, BN) : 0;
+  p.flags_per_chunk = p.splits > 1 ? 4 * cdiv(C, PAIR_M) * cdiv(H, BN) : 0;   // (tile, CTA, warpgroup)
   p.n_counters = p.n_chunks * (2 + p.flags_per_chunk);   // tile counters, then split flags
   size_t off = al256(HDR_WORDS * sizeof(int));
   p.o_idx = off;  off += al256(size_t(N) * 4);
@@ -120,7 +121,7 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
   p.o_xc = off;   off += al256(size_t(C) * H * 2);
   p.o_tc = off;   off += al256(size_t(C) * 4);
   p.o_zt = off;   off += al256(size_t(C) * 4);
-  p.o_part = off; off += al256(size_t(C) * p.nvt * 8);
+  p.o_part = off; off += al256(size_t(C) * p.nparts * 8);
   if (!fwd_only) {
     p.o_z = off; off += al256(size_t(C) * p.ldz * 2);
     if (p.splits > 1) { p.o_dx = off; off += al256(size_t(C) * H * 4); }
@@ -188,7 +189,8 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 bool make_map(CUtensorMap* m, const void* base, unsigned long long inner, unsigned long long outer,
               unsigned long long row_bytes, unsigned box_inner, unsigned box_outer,
-              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -196,7 +198,7 @@ bool make_map(CUtensorMap* m, const void* base, unsigned long long inner, unsign
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -298,10 +300,12 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   if (!fwd_only)
     ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, weight, H, V, hb, 64, BK) &&
          make_map(&bm.a1, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&bm.b1, xc, H, p.C, hb, 64, BK) &&
-         make_map(&bm.out, grad_weight, H, V, static_cast<unsigned long long>(H) * 4, 32, BM,
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32) &&
-         (!dxacc || make_map(&bm.dx, dxacc, H, p.C, static_cast<unsigned long long>(H) * 4, 32, BM,
-                             CU_TENSOR_MAP_DATA_TYPE_FLOAT32));
+         make_map(&bm.out, grad_weight, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+         make_map(&bm.pf, grad_weight, H, V, static_cast<unsigned long long>(H) * 4, BN, BM,
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         (!dxacc || make_map(&bm.dx, dxacc, H, p.C, static_cast<unsigned long long>(H) * 4, 16, BM,
+                             CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B));
   if (!ok) return FLCE_ECUDA;
 
   const int reduce_sum = (flags & FLCE_REDUCE_SUM) ? 1 : 0;
@@ -314,6 +318,7 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   g.V = static_cast<int>(V);
   g.ldz = p.ldz;
   g.nvt = p.nvt;
+  g.nparts = p.nparts;
   g.store_z = fwd_only ? 0 : 1;
   g.timeout_ns = wait_timeout_ns();
   g.z = z;
@@ -349,7 +354,7 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
     g.mode = MODE_LOGITS;
     g.counter = sync;
     if (!chk(gemm_launch(g, fm, grid_logits, st))) return FLCE_ECUDA;
-    if (!chk(launch_lse_dz(hdr, c0, g.C, g.V, p.ldz, p.nvt, part, zt, tc, rl, z, reduce_sum, fwd_only ? 0 : 1,
+    if (!chk(launch_lse_dz(hdr, c0, g.C, g.V, p.ldz, p.nparts, part, zt, tc, rl, z, reduce_sum, fwd_only ? 0 : 1,
                            st)))
       return FLCE_ECUDA;
     if (fwd_only) continue;

@@ -7,7 +7,7 @@
 //   zero        grad_hidden rows of ignored tokens = +0.0
 //   gather      copy one chunk of valid hidden rows (and their targets) into
 //               a dense [C, H] tile source; padding rows are zero
-//   lse_dz      merge the per-tile (max, sum exp) pairs of each row into
+//   lse_dz      merge the per-part (max, sum exp) pairs of each row into
 //               log-sum-exp in a fixed order, emit loss_n = lse_n - z_t, and
 //               turn the stored shifted logits into dz = (softmax - onehot) * s
 //               in place ("gradient of softmax + CE loss": softmax minus the
@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restric
     hdr[HDR_STATUS] = bad ? STATUS_BADTARGET : 0;
     hdr[HDR_NVALID] = total;
     hdr[HDR_STALL] = 0;
+    hdr[HDR_STALL_COUNT] = 0;
     if (n_valid_out) *n_valid_out = total;
   }
 }
@@ -145,7 +146,7 @@ __global__ void gather_kernel(const uint16_t* __restrict__ X, const int* __restr
 constexpr int LSE_THREADS = 256;
 
 __global__ void __launch_bounds__(LSE_THREADS)
-    lse_dz_kernel(const int* hdr, long long c0, int C, int V, long long ldz, int nvt,
+    lse_dz_kernel(const int* hdr, long long c0, int C, int V, long long ldz, int nparts,
                   const float2* __restrict__ part, const float* __restrict__ zt, const int* __restrict__ tc,
                   float* __restrict__ rl, uint16_t* __restrict__ z, int reduce_sum, int make_dz) {
   __shared__ float red[LSE_THREADS / 32];
@@ -161,12 +162,12 @@ __global__ void __launch_bounds__(LSE_THREADS)
         *reinterpret_cast<uint4*>(zr + v) = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  const float2* pr = part + static_cast<size_t>(r) * nvt;
+  const float2* pr = part + static_cast<size_t>(r) * nparts;
   float m = -INFINITY;
-  for (int j = tid; j < nvt; j += LSE_THREADS) m = fmaxf(m, pr[j].x);
+  for (int j = tid; j < nparts; j += LSE_THREADS) m = fmaxf(m, pr[j].x);
   m = block_reduce(m, MaxOp(), -INFINITY, red);
   float d = 0.f;
-  for (int j = tid; j < nvt; j += LSE_THREADS) d += pr[j].y * exp2f((pr[j].x - m) * LOG2E);
+  for (int j = tid; j < nparts; j += LSE_THREADS) d += pr[j].y * exp2f((pr[j].x - m) * LOG2E);
   d = block_reduce(d, AddOp(), 0.f, red);
   const float lse = m + logf(d);
   if (tid == 0) rl[c0 + r] = lse - zt[r];
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(LSE_THREADS)
   const float scale = reduce_sum ? 1.f : 1.f / static_cast<float>(nv);
   const int tgt = tc[r];
   // four 8-column groups in flight per thread; each group lies in one
-  // 256-wide tile, where z = stored value + tile max
+  // 128-column part, where z = stored value + part max
   constexpr long long STEP = LSE_THREADS * 8LL;
   for (long long v0 = tid * 8LL; v0 < ldz; v0 += 4 * STEP) {
     uint4 w[4];
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(LSE_THREADS)
       if (v >= ldz) break;
       uint4 o = make_uint4(0u, 0u, 0u, 0u);
       if (v < V) {
-        const float b2 = (pr[v / BN].x - lse) * LOG2E;
+        const float b2 = (pr[v / PART_COLS].x - lse) * LOG2E;
         const uint32_t in[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
         uint32_t out[4];
 #pragma unroll
@@ -272,10 +273,10 @@ cudaError_t launch_gather(const uint16_t* hidden, const int* targets, const int*
   return cudaGetLastError();
 }
 
-cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long ldz, int nvt,
+cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long ldz, int nparts,
                           const float2* part, const float* zt, const int* tc, float* rl, uint16_t* z,
                           int reduce_sum, int make_dz, cudaStream_t s) {
-  lse_dz_kernel<<<C, LSE_THREADS, 0, s>>>(hdr, c0, C, V, ldz, nvt, part, zt, tc, rl, z, reduce_sum, make_dz);
+  lse_dz_kernel<<<C, LSE_THREADS, 0, s>>>(hdr, c0, C, V, ldz, nparts, part, zt, tc, rl, z, reduce_sum, make_dz);
   return cudaGetLastError();
 }
 

@@ -40,11 +40,16 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STG_BYTES = BM * 32 * 4;      // one 128 x 32 fp32 slice of an output tile
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_THREADS = 128;
+constexpr int SLICE_COLS = 16;              // fp32 columns per staged output slice (64 B rows)
+constexpr int STG_BYTES = BM * SLICE_COLS * 4;   // one 128 x 16 fp32 slice: 8 KB
+constexpr int EPI_GROUPS = 2;               // epilogue warpgroups, one per 128-column half
+constexpr int GROUP_COLS = BN / EPI_GROUPS;
+constexpr int GROUP_THREADS = 128;
+constexpr int EPI_THREADS = EPI_GROUPS * GROUP_THREADS;
+constexpr int NUM_THREADS = 64 + EPI_THREADS;   // warp 0 TMA, warp 1 MMA, then the epilogue warps
 constexpr int SCHED_SLOTS = 4;
-constexpr uint32_t EPI_BAR = 1;             // named barrier of the epilogue warps
+constexpr uint32_t EPI_BAR_ALL = 1;         // named barrier of all epilogue warps
+constexpr uint32_t EPI_BAR_GROUP = 2;       // + warpgroup index: per-warpgroup named barrier
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MN_BLOCK_BYTES = 64 * 128;    // 64 K rows x 128 B (64 bf16 along M or N)
 constexpr uint16_t PAIR_MASK = 0x3;
@@ -64,7 +69,7 @@ struct Ctl {
 };
 
 constexpr int CTL_BYTES = ((sizeof(Ctl) + 255) / 256) * 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * STG_BYTES + CTL_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * EPI_GROUPS * STG_BYTES + CTL_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Readers of a scheduler slot: in CTA 0 the MMA lane and its epilogue
@@ -80,13 +85,19 @@ enum WaitSite : int {
   W_TMEM_EMPTY = 6, W_STAGE_FULL = 7, W_MMA_DONE = 8, W_SCHED_FULL_EPI = 9, W_TMEM_FULL = 10, W_SPLIT_FLAG = 11
 };
 
-__device__ void record_stall(int* hdr, int site) {
+// detail: the tile being worked on (or -1) and the ring position waited on
+__device__ void record_stall(int* hdr, int site, int detail) {
   const int code = site | (static_cast<int>(ptx::cluster_ctarank()) << 8) | (static_cast<int>(blockIdx.x) << 12);
   atomicCAS(hdr + HDR_STALL, 0, code);
+  const int k = atomicAdd(hdr + HDR_STALL_COUNT, 1);
+  if (k < STALL_LOG_MAX) {
+    hdr[HDR_STALL_LOG + 2 * k] = code;
+    hdr[HDR_STALL_LOG + 2 * k + 1] = detail;
+  }
 }
 
 __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Ctl* ctl, uint64_t timeout_ns,
-                                        bool honor_abort, int* hdr, int site) {
+                                        bool honor_abort, int* hdr, int site, int detail = -1) {
   if (ptx::mbar_test_cluster(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -95,7 +106,7 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Ctl* ctl
       if (honor_abort && *reinterpret_cast<volatile int*>(&ctl->abort)) return false;
       if (ptx::global_timer_ns() - t0 > timeout_ns) {
         *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-        record_stall(hdr, site);
+        record_stall(hdr, site, detail);
         return false;
       }
     }
@@ -112,7 +123,7 @@ __device__ __noinline__ bool wait_flag(const int* flag, int target, Ctl* ctl, ui
       if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
       if (ptx::global_timer_ns() - t0 > timeout_ns) {
         *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
-        record_stall(hdr, W_SPLIT_FLAG);
+        record_stall(hdr, W_SPLIT_FLAG, target);
         return false;
       }
     }
@@ -186,20 +197,24 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const Shape& s, i
 }
 
 // ---------------------------------------------------------------------------
-// epilogues (one thread = one accumulator row of this CTA; tbase = this warp's
-// TMEM lanes; row0 = first row of this CTA's half of the pair tile)
+// epilogues: one thread = one accumulator row of this CTA; each warpgroup owns
+// 128 of the 256 columns.  tbase = this warp's TMEM lanes at the warpgroup's
+// first column; row0 = first row of this CTA's half of the pair tile; col0 =
+// first column of the warpgroup inside the tile.
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, const Unit& t, int row0,
+__device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, const Unit& t, int row0, int col0,
                                            uint32_t tbase, int r) {
   const int grow = row0 + r;
   const bool rv = grow < s.Cl;
+  const int c0 = t.n0 + col0;                     // first vocabulary column of this part
   const int tgt = rv ? a.tc[grow] : -1;
-  const int tl = tgt - t.n0;
-  const int ncol = min(BN, a.V - t.n0);
+  const int tl = tgt - c0;
+  const int ncol = min(GROUP_COLS, a.V - c0);     // may be <= 0 past the vocabulary
+  if (ncol <= 0) return;                          // uniform over the warpgroup
   float mx = -INFINITY, ztv = 0.f;
 #pragma unroll 1
-  for (int j = 0; j < BN / 32; ++j) {
+  for (int j = 0; j < GROUP_COLS / 32; ++j) {
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
 #pragma unroll
@@ -210,10 +225,10 @@ __device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, co
     }
   }
   float sum = 0.f;
-  uint16_t* zrow = a.z + static_cast<size_t>(grow) * a.ldz + t.n0;
+  uint16_t* zrow = a.z + static_cast<size_t>(grow) * a.ldz + c0;
   const bool store = a.store_z && rv;
 #pragma unroll 1
-  for (int j = 0; j < BN / 32; ++j) {
+  for (int j = 0; j < GROUP_COLS / 32; ++j) {
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
     uint32_t pk[16];
@@ -225,14 +240,14 @@ __device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, co
       if (c + 1 < ncol) sum += exp2f(s1 * LOG2E);
       pk[k / 2] = ptx::pack_bf16x2(s0, s1);
     }
-    if (store && t.n0 + j * 32 < a.ldz) {
+    if (store && c0 + j * 32 < a.ldz) {
       uint4* dst = reinterpret_cast<uint4*>(zrow + j * 32);
 #pragma unroll
       for (int g = 0; g < 4; ++g) dst[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
     }
   }
   if (rv) {
-    a.part[static_cast<size_t>(grow) * a.nvt + t.ntile] = make_float2(mx, sum);
+    a.part[static_cast<size_t>(grow) * a.nparts + c0 / PART_COLS] = make_float2(mx, sum);
     if (tl >= 0 && tl < ncol) a.zt[grow] = ztv;
   }
 }
@@ -249,14 +264,14 @@ __device__ __forceinline__ void store_bf16_row(uint16_t* dst, const float* v, in
   }
 }
 
-__device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s, const Unit& t, int row0,
+__device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s, const Unit& t, int row0, int col0,
                                               uint32_t tbase, int r) {
   const int grow = row0 + r;
   const bool rv = grow < s.Cl;
   const long long tok = rv ? a.idx[a.c0 + grow] : 0;
 #pragma unroll 1
-  for (int j = 0; j < BN / 32; ++j) {
-    const int h = t.n0 + j * 32;
+  for (int j = 0; j < GROUP_COLS / 32; ++j) {
+    const int h = t.n0 + col0 + j * 32;
     if (h >= a.H) break;  // warp-uniform
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
@@ -264,29 +279,30 @@ __device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s,
   }
 }
 
-// One 128 x 256 fp32 accumulator half -> 32-column slices -> shared memory
-// (128-byte swizzled rows, conflict-free) -> TMA store (reduce == false) or
-// TMA reduce-add into `map` at (n0 + 32 j, row0).  Two staging buffers
-// alternate; `leader` owns the bulk-group bookkeeping.
-__device__ __forceinline__ void tile_to_global(const CUtensorMap* map, int ncols_total, int n0, int row0,
-                                               bool reduce, uint32_t tbase, int r, bool leader, uint8_t* stg,
-                                               uint32_t& stg_count) {
+// The warpgroup's 128 x 128 fp32 accumulator block -> 16-column slices ->
+// shared memory (64-byte rows, 64-byte swizzle: chunk g of row r sits at
+// g ^ ((r >> 1) & 3), conflict-free) -> TMA store (reduce == false) or TMA
+// reduce-add into `map` at (h, row0).  Two staging buffers per warpgroup
+// alternate; `leader` (one thread of the warpgroup) owns the bulk groups.
+__device__ __forceinline__ void block_to_global(const CUtensorMap* map, int ncols_total, int h0, int row0,
+                                                bool reduce, uint32_t tbase, int r, bool leader, uint32_t bar,
+                                                uint8_t* stg, uint32_t& stg_count) {
 #pragma unroll 1
-  for (int j = 0; j < BN / 32; ++j) {
-    const int h = n0 + j * 32;
-    if (h >= ncols_total) break;  // uniform over the epilogue warps
-    float v[32];
-    ptx::tmem_ld32(tbase + j * 32, v);
+  for (int j = 0; j < GROUP_COLS / SLICE_COLS; ++j) {
+    const int h = h0 + j * SLICE_COLS;
+    if (h >= ncols_total) break;  // uniform over the warpgroup
+    float v[SLICE_COLS];
+    ptx::tmem_ld16(tbase + j * SLICE_COLS, v);
     uint8_t* buf = stg + (stg_count & 1u) * STG_BYTES;
     if (leader) ptx::bulk_wait_read_1();          // the store that last used `buf` has read it
-    ptx::named_bar_sync(EPI_BAR, EPI_THREADS);
-    uint8_t* row = buf + r * 128;
+    ptx::named_bar_sync(bar, GROUP_THREADS);
+    uint8_t* row = buf + r * (SLICE_COLS * 4);
 #pragma unroll
-    for (int g = 0; g < 8; ++g)
-      *reinterpret_cast<float4*>(row + ((g ^ (r & 7)) << 4)) =
+    for (int g = 0; g < 4; ++g)
+      *reinterpret_cast<float4*>(row + ((g ^ ((r >> 1) & 3)) << 4)) =
           make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
     ptx::fence_proxy_async_smem();
-    ptx::named_bar_sync(EPI_BAR, EPI_THREADS);
+    ptx::named_bar_sync(bar, GROUP_THREADS);
     if (leader) {
       if (reduce)
         ptx::tma_reduce_add_2d(map, buf, h, row0);
@@ -300,18 +316,21 @@ __device__ __forceinline__ void tile_to_global(const CUtensorMap* map, int ncols
 
 // dX unit of a split vocabulary: split 0 stores its fp32 part, split k waits
 // until split k-1 has landed and reduce-adds onto it, the last split turns
-// the finished fp32 rows into bf16 grad_hidden rows.  Returns false on abort.
+// the finished fp32 rows into bf16 grad_hidden rows.  Each warpgroup orders
+// its own column half.  Returns false on abort.
 __device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* maps, const Shape& s,
-                                             const Unit& t, int row0, uint32_t rank, uint32_t tbase, int r,
-                                             bool leader, uint8_t* stg, uint32_t& stg_count, Ctl* ctl) {
-  int* flag = a.flags + 2 * t.ntile + rank;
+                                             const Unit& t, int row0, int col0, int grp, uint32_t rank,
+                                             uint32_t tbase, int r, bool leader, uint32_t bar, uint8_t* stg,
+                                             uint32_t& stg_count, Ctl* ctl) {
+  int* flag = a.flags + 4 * t.ntile + 2 * static_cast<int>(rank) + grp;
   bool ok = true;
   if (leader && t.split > 0) {
     ok = wait_flag(flag, t.split, ctl, a.timeout_ns, const_cast<int*>(a.hdr));
     ptx::fence_proxy_async_global();
   }
-  if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) return false;
-  tile_to_global(&maps->dx, a.H, t.n0, row0, t.split > 0, tbase, r, leader, stg, stg_count);
+  if (!ptx::named_bar_and(bar, GROUP_THREADS, ok)) return false;
+  const int h0 = t.n0 + col0;
+  block_to_global(&maps->dx, a.H, h0, row0, t.split > 0, tbase, r, leader, bar, stg, stg_count);
   if (leader) {
     ptx::bulk_wait_all();                 // this part has landed in global memory
     ptx::fence_proxy_async_global();
@@ -319,13 +338,13 @@ __device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* 
     ptx::st_release_gpu(flag, t.split + 1);
   }
   if (t.split == a.splits - 1) {
-    ptx::named_bar_sync(EPI_BAR, EPI_THREADS);
+    ptx::named_bar_sync(bar, GROUP_THREADS);
     const int grow = row0 + r;
     if (grow < s.Cl) {
       const long long tok = a.idx[a.c0 + grow];
       const float* src = a.dxacc + static_cast<size_t>(grow) * a.H;
-      for (int j = 0; j < BN / 32; ++j) {
-        const int h = t.n0 + j * 32;
+      for (int j = 0; j < GROUP_COLS / 32; ++j) {
+        const int h = h0 + j * 32;
         if (h >= a.H) break;
         float v[32];
 #pragma unroll
@@ -344,14 +363,12 @@ __device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* 
   return true;
 }
 
-// ---------------------------------------------------------------------------
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     flce_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg = smem + STAGES * STAGE_BYTES;
-  Ctl* ctl = reinterpret_cast<Ctl*>(stg + 2 * STG_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(stg + 2 * EPI_GROUPS * STG_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ptx::cluster_ctarank();
   const bool lead = rank == 0;
@@ -377,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ctl->tfull[i], 1);
-      ptx::mbar_init(&ctl->tempty[i], 2 * EPI_THREADS);
+      ptx::mbar_init(&ctl->tempty[i], 2 * EPI_THREADS);   // both CTAs' epilogue threads
     }
     for (int i = 0; i < SCHED_SLOTS; ++i) {
       ptx::mbar_init(&ctl->sfull[i], 1);
@@ -392,6 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       ptx::tma_prefetch_desc(&maps.a1);
       ptx::tma_prefetch_desc(&maps.b1);
       ptx::tma_prefetch_desc(&maps.out);
+      ptx::tma_prefetch_desc(&maps.pf);
       if (a.splits > 1) ptx::tma_prefetch_desc(&maps.dx);
     }
   }
@@ -431,8 +449,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
+      // the epilogue of a dW unit reduce-adds into grad_weight: pull this
+      // CTA's 128 x 256 block of it into L2 while the main loop runs
+      if (t.kind == U_DW && a.accumulate) ptx::tma_prefetch_l2_2d(&maps.pf, t.n0, t.m0 + half);
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        if (!wait_phase(&ctl->empty[stage], phase ^ 1u, ctl, to, true, hdr, W_STAGE_EMPTY)) { ok = false; break; }
+        if (!wait_phase(&ctl->empty[stage], phase ^ 1u, ctl, to, true, hdr, W_STAGE_EMPTY, u | (stage << 24))) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         const uint32_t fb = ptx::map_to_rank(&ctl->full[stage], 0);   // CTA 0's barrier
@@ -480,12 +501,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t idesc = ptx::idesc_bf16_f32(PAIR_M, BN, a_mn, b_mn);
       const uint32_t a_lbo = a_mn ? MN_BLOCK_BYTES : 16, b_lbo = b_mn ? MN_BLOCK_BYTES : 16;
       const uint32_t a_kstep = a_mn ? 16 * 128 : 32, b_kstep = b_mn ? 16 * 128 : 32;
-      if (!wait_phase(&ctl->tempty[acc], acc_phase ^ 1u, ctl, to, true, hdr, W_TMEM_EMPTY)) break;
+      if (!wait_phase(&ctl->tempty[acc], acc_phase ^ 1u, ctl, to, true, hdr, W_TMEM_EMPTY, u | (acc << 24))) break;
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem + acc * BN;
       bool ok = true;
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        if (!wait_phase(&ctl->full[stage], phase, ctl, to, true, hdr, W_STAGE_FULL)) { ok = false; break; }
+        if (!wait_phase(&ctl->full[stage], phase, ctl, to, true, hdr, W_STAGE_FULL, u | (stage << 24))) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t sb = sa + A_BYTES;
@@ -506,41 +527,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ptx::umma_commit_pair(&ctl->mma_done, 0x1);
     wait_phase(&ctl->mma_done, 0, ctl, to, false, hdr, W_MMA_DONE);
   } else if (warp >= 2) {
-    // ---------------- epilogue (both CTAs: 128 rows each) ----------------
-    const int q = warp & 3;             // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;        // accumulator row within this CTA's half
-    const bool leader = warp == 2 && lane == 0;
+    // ---------------- epilogue (both CTAs: 128 rows each, two warpgroups) ----------------
+    const int q = warp & 3;                   // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;              // accumulator row within this CTA's half
+    const int grp = (warp - 2) / 4;           // warpgroup: column half of the tile
+    const int col0 = grp * GROUP_COLS;
+    const bool leader = ((warp - 2) & 3) == 0 && lane == 0;
+    const uint32_t gbar = EPI_BAR_GROUP + static_cast<uint32_t>(grp);
+    uint8_t* gstg = stg + grp * 2 * STG_BYTES;
     const uint32_t sempty0 = ptx::map_to_rank(&ctl->sempty[0], 0);
     const uint32_t tempty0 = ptx::map_to_rank(&ctl->tempty[0], 0);
     uint32_t acc = 0, acc_phase = 0, sslot = 0, sphase = 0, stg_count = 0;
     for (;;) {
       // every wait is followed by a vote so that all epilogue threads leave together
-      bool ok = wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_EPI);
-      if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) break;
+      bool ok = wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_EPI, sslot << 24);
+      if (!ptx::named_bar_and(EPI_BAR_ALL, EPI_THREADS, ok)) break;
       const int u = ctl->sunit[sslot];
       ptx::mbar_arrive_remote(sempty0 + sslot * 8u);
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
-      ok = wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true, hdr, W_TMEM_FULL);
-      if (!ptx::named_bar_and(EPI_BAR, EPI_THREADS, ok)) break;
+      ok = wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true, hdr, W_TMEM_FULL, u | (acc << 24));
+      if (!ptx::named_bar_and(EPI_BAR_ALL, EPI_THREADS, ok)) break;
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + col0;
       const int row0 = t.m0 + half;
       bool cont = true;
       if (t.kind == U_LOGITS)
-        epi_logits(a, s, t, row0, tbase, r);
+        epi_logits(a, s, t, row0, col0, tbase, r);
       else if (t.kind == U_DX && a.splits == 1)
-        epi_dx_direct(a, s, t, row0, tbase, r);
+        epi_dx_direct(a, s, t, row0, col0, tbase, r);
       else if (t.kind == U_DX)
-        cont = epi_dx_split(a, &maps, s, t, row0, rank, tbase, r, leader, stg, stg_count, ctl);
+        cont = epi_dx_split(a, &maps, s, t, row0, col0, grp, rank, tbase, r, leader, gbar, gstg, stg_count, ctl);
       else
-        tile_to_global(&maps.out, a.H, t.n0, row0, a.accumulate != 0, tbase, r, leader, stg, stg_count);
+        block_to_global(&maps.out, a.H, t.n0 + col0, row0, a.accumulate != 0, tbase, r, leader, gbar, gstg,
+                        stg_count);
       ptx::tc_fence_before();
       ptx::mbar_arrive_remote(tempty0 + acc * 8u);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
-      if (!cont) break;
+      if (!ptx::named_bar_and(EPI_BAR_ALL, EPI_THREADS, cont)) break;
     }
     if (leader) ptx::bulk_wait_all();
   }

@@ -15,6 +15,9 @@ constexpr int STATUS_TIMEOUT = 2;
 constexpr int HDR_STATUS = 0;
 constexpr int HDR_NVALID = 1;
 constexpr int HDR_STALL = 2;   // first pipeline wait that timed out: site | rank << 8 | block << 12
+constexpr int HDR_STALL_COUNT = 3;   // number of timed-out waits
+constexpr int HDR_STALL_LOG = 8;     // up to 8 records (code, detail) of timed-out waits
+constexpr int STALL_LOG_MAX = 8;
 constexpr int HDR_WORDS = 64;
 
 // GEMM tile shape: a CTA pair (cluster of 2, tcgen05 cta_group::2) owns a
@@ -24,6 +27,9 @@ constexpr int BM = 128;
 constexpr int PAIR_M = 2 * BM;
 constexpr int BN = 256;
 constexpr int BK = 64;
+// The logits epilogue keeps one (max, sum exp) pair per row and 128-column
+// vocabulary part (each epilogue warpgroup owns half of a 256-column tile).
+constexpr int PART_COLS = 128;
 
 enum GemmMode : int {
   MODE_LOGITS = 0,  // z = Xc W^T, epilogue: per-tile (max, sum exp), z_t, shifted bf16 logits
@@ -41,17 +47,18 @@ struct GemmArgs {
   int C;                // chunk capacity (rows)
   int H, V;
   long long ldz;        // row stride (elements) of the chunk logits buffer
-  int nvt;              // ceil(V / BN)
+  int nvt;              // vocabulary tiles: ceil(V / BN)
+  int nparts;           // vocabulary parts: ceil(V / PART_COLS)
   int store_z;          // LOGITS: write the shifted bf16 logits
   int accumulate;       // BWD: add into grad_weight (chunks after the first)
   int first_chunk;      // BWD: chunk 0 (writes zeros when it is empty)
   int splits;           // BWD: vocabulary splits of the grad_hidden GEMM
   int kb_per_split;     // BWD: K blocks per split
-  int* flags;           // BWD, splits > 1: per (tile, CTA) count of finished splits (zero before)
+  int* flags;           // BWD, splits > 1: per (tile, CTA, warpgroup) count of finished splits (zero before)
   unsigned long long timeout_ns;
   // epilogue operands
   uint16_t* z;          // [C][ldz] bf16
-  float2* part;         // [C][nvt] (tile max, tile sum of exp)
+  float2* part;         // [C][nparts] (part max, part sum of exp)
   float* zt;            // [C] target logit
   const int* tc;        // [C] chunk targets (-1 for padding rows)
   const int* idx;       // [N] compacted row -> token row
@@ -62,10 +69,11 @@ struct GemmArgs {
 
 // Tensor maps of one launch.  LOGITS: a0 = Xc (K-major), b0 = W (K-major).
 // BWD: a0 = dz (K-major), b0 = W (MN-major), a1 = dz (MN-major view),
-// b1 = Xc (MN-major), out = grad_weight (fp32, store / reduce-add),
-// dx = the fp32 grad_hidden split accumulator (store / reduce-add).
+// b1 = Xc (MN-major), out = grad_weight (fp32, store / reduce-add of 16 x 128
+// slices), dx = the fp32 grad_hidden split accumulator (same slices),
+// pf = grad_weight again with a 256 x 128 box for L2 prefetches.
 struct GemmMaps {
-  CUtensorMap a0, b0, a1, b1, out, dx;
+  CUtensorMap a0, b0, a1, b1, out, dx, pf;   // pf: grad_weight, 256 x 128 box, L2 prefetch
 };
 
 int gemm_smem_bytes();
@@ -83,7 +91,7 @@ cudaError_t launch_gather(const uint16_t* hidden, const int* targets, const int*
                           const int* idx, long long c0, int C, int H,
                           uint16_t* xc, int* tc, cudaStream_t s);
 cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long ldz,
-                          int nvt, const float2* part, const float* zt, const int* tc,
+                          int nparts, const float2* part, const float* zt, const int* tc,
                           float* rl, uint16_t* z, int reduce_sum, int make_dz,
                           cudaStream_t s);
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl,

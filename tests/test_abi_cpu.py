@@ -72,9 +72,9 @@ def test_plan_monotone_and_minimum(lib):
     with pytest.raises(flce.FlceError) as e:
         flce.plan(N, H, V, 4096)
     assert e.value.status == flce.FLCE_EWORKSPACE
-    # forward-only needs no logits buffer: the whole batch fits in one chunk
-    f = flce.workspace_bytes(N, H, V, forward_only=True)
-    assert flce.plan(N, H, V, f, forward_only=True)["chunk_rows"] == 1024
+    # forward-only needs no logits buffer: the same bytes hold a larger chunk
+    f = flce.workspace_bytes(N, H, V)
+    assert flce.plan(N, H, V, f, forward_only=True)["chunk_rows"] >= flce.plan(N, H, V, f)["chunk_rows"]
 
 
 def test_bad_arguments_rejected_on_host(lib):
