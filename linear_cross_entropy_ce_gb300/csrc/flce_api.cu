@@ -97,7 +97,7 @@ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 constexpr int DEFAULT_PAIRS = 76;
-constexpr int MAX_SPLITS = 16;
+constexpr int MAX_SPLITS = 8;   // splits are summed one after another: keep the chain short
 
 // Workspace layout for chunks of C rows.  Only the bf16 C x V logits buffer
 // (absent for the forward-only call) grows with V.
@@ -134,10 +134,11 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
 // tile (K = V) should take at most half of a pair's average share of the
 // backward launch, or it alone sets the launch's length.
 int preferred_splits(long long C, long long H, long long V, int pairs) {
-  const double mt = double(cdiv(C, PAIR_M)), nt = double(cdiv(H, BN));
-  const double work = mt * nt * double(V) + double(cdiv(V, PAIR_M)) * nt * double(C);
+  const double dx_tiles = double(cdiv(C, PAIR_M)) * double(cdiv(H, BN));
+  const double unit = double(PAIR_M) * BN * double(V);
+  const double work = dx_tiles * unit + double(cdiv(V, PAIR_M)) * double(cdiv(H, BN)) * PAIR_M * BN * double(C);
   const double per_pair = work / double(pairs);
-  long long S = static_cast<long long>(std::ceil(double(V) / (0.5 * per_pair)));
+  long long S = static_cast<long long>(std::ceil(unit / (0.5 * per_pair)));
   const long long max_by_k = std::max<long long>(1, cdiv(V, BK) / 8);   // >= 8 K blocks per split
   S = std::min<long long>(std::min<long long>(S, MAX_SPLITS), max_by_k);
   return static_cast<int>(std::max<long long>(S, 1));
