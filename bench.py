@@ -35,6 +35,16 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and % of GB300 dense BF16 tensor peak
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def kernel_sources_sha1() -> str:
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    for f in sorted(glob.glob(os.path.join(ROOT, "linear_cross_entropy_ce_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -316,7 +326,9 @@ def main():
     if os.path.exists(tpath):
         try:
             tj = json.load(open(tpath))
-            if tj.get("workload") == w.name and tj.get("kernel_build") == flce.version():
+            # only valid for the kernel sources the counters were taken on
+            if tj.get("workload") == w.name and tj.get("kernel_sources_sha1") == kernel_sources_sha1() \
+                    and not args.tokens and not args.chunk_rows:
                 traffic = tj.get("dram_bytes_per_launch")
         except Exception:
             traffic = None
