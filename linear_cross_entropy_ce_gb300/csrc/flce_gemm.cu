@@ -48,6 +48,7 @@ constexpr int GROUP_THREADS = 128;
 constexpr int EPI_THREADS = EPI_GROUPS * GROUP_THREADS;
 constexpr int NUM_THREADS = 64 + EPI_THREADS;   // warp 0 TMA, warp 1 MMA, then the epilogue warps
 constexpr int SCHED_SLOTS = 4;
+constexpr int SHORT_TILE_KB = 32;           // tiles with at most this many K blocks claim their successor early
 constexpr uint32_t EPI_BAR_ALL = 1;         // named barrier of all epilogue warps
 constexpr uint32_t EPI_BAR_GROUP = 2;       // + warpgroup index: per-warpgroup named barrier
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -431,12 +432,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t stage = 0, phase = 0, sslot = 0, sphase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
+    // CTA 0 claims tiles from the global counter.  After a short tile the
+    // claim latency would stall the ring between tiles, so the next tile is
+    // claimed as soon as a short tile starts (its loads hide the atomic); a
+    // long tile claims its successor only when its own loads are all issued,
+    // so that it never holds work another pair could start.
+    int next = lead ? atomicAdd(a.counter, 1) : -1;
     for (;;) {
       int u;
       if (lead) {
         if (!wait_phase(&ctl->sempty[sslot], sphase ^ 1u, ctl, to, true, hdr, W_SCHED_EMPTY)) { ok = false; break; }
-        u = atomicAdd(a.counter, 1);
-        if (u >= s.units) u = -1;
+        if (next < 0) next = atomicAdd(a.counter, 1);
+        u = next < s.units ? next : -1;
+        next = -1;
         ctl->sunit[sslot] = u;
         ptx::st_remote_u32(ptx::map_to_rank(&ctl->sunit[sslot], 1), static_cast<uint32_t>(u));
         ptx::mbar_arrive(&ctl->sfull[sslot]);
@@ -452,6 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // the epilogue of a dW unit reduce-adds into grad_weight: pull this
       // CTA's 128 x 256 block of it into L2 while the main loop runs
       if (t.kind == U_DW && a.accumulate) ptx::tma_prefetch_l2_2d(&maps.pf, t.n0, t.m0 + half);
+      if (lead && t.kb1 - t.kb0 <= SHORT_TILE_KB) next = atomicAdd(a.counter, 1);
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
         if (!wait_phase(&ctl->empty[stage], phase ^ 1u, ctl, to, true, hdr, W_STAGE_EMPTY, u | (stage << 24))) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
