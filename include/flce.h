@@ -138,6 +138,20 @@ flce_status flce_loss(const void* hidden, const void* weight,
                       size_t workspace_bytes, void* stream);
 
 /*
+ * grad_hidden (bf16 [N,H]) and grad_weight (fp32 [V,H]) multiplied in place by
+ * the fp32 scalar at device address `scale` (read on the device, so the call
+ * does not synchronise).  This is the backward of the fused op inside an
+ * autograd graph: flce_fwd_bwd already produced the gradients of the loss, and
+ * the backward pass only scales them by the incoming gradient of the loss
+ * ("efficient-llm-anatomy" README, "Fused cross-entropy computes backward
+ * during forward": the backward pass just distributes them).  H % 8 == 0;
+ * pointers 16-byte aligned (scale 4-byte).
+ */
+flce_status flce_scale_grads(void* grad_hidden, float* grad_weight, int64_t N,
+                             int64_t H, int64_t V, const float* scale,
+                             void* stream);
+
+/*
  * Synchronises `stream`, then reads the device status word of the last call
  * that used `workspace`: FLCE_OK, FLCE_EBADTARGET or FLCE_ETIMEOUT (or
  * FLCE_ECUDA if the stream reports an error).

@@ -450,6 +450,19 @@ flce_status flce_query_status(const void* workspace, void* stream) {
   return FLCE_OK;
 }
 
+flce_status flce_scale_grads(void* grad_hidden, float* grad_weight, int64_t N, int64_t H, int64_t V,
+                             const float* scale, void* stream) {
+  if (!grad_hidden || !grad_weight || !scale) return FLCE_EINVAL;
+  if (N < 1 || H < 1 || V < 1) return FLCE_EINVAL;
+  if (!sizes_ok(N, H, V)) return FLCE_EUNSUPPORTED;
+  if (!aligned16(grad_hidden) || !aligned16(grad_weight) || !aligned4(scale)) return FLCE_EUNSUPPORTED;
+  count_launches(1);
+  if (launch_scale_grads(static_cast<uint16_t*>(grad_hidden), N * H, grad_weight, V * H, scale,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FLCE_ECUDA;
+  return FLCE_OK;
+}
+
 flce_status flce_selftest_timeout(void* workspace, uint64_t timeout_ns, void* stream) {
   if (!workspace || !aligned16(workspace) || timeout_ns == 0 || timeout_ns > 10000000000ull) return FLCE_EINVAL;
   if (launch_timeout_selftest(static_cast<int*>(workspace), timeout_ns, static_cast<cudaStream_t>(stream)) !=

@@ -231,6 +231,30 @@ __global__ void __launch_bounds__(FIN_THREADS)
     for (long long i = threadIdx.x; i < N; i += FIN_THREADS) row_loss[idx[i]] = i < nv ? rl[i] : 0.f;
 }
 
+// grad_hidden (bf16) and grad_weight (fp32) times a device scalar, in place:
+// the backward of the fused op when the incoming gradient of the loss is not
+// one ("efficient-llm-anatomy" README: the backward pass only distributes the
+// gradients computed during forward).
+__global__ void scale_grads_kernel(uint16_t* __restrict__ gh, long long n8, float* __restrict__ gw, long long n4,
+                                   const float* __restrict__ scale) {
+  const float a = *scale;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    uint4 w = reinterpret_cast<uint4*>(gh)[i];
+    uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      out[g] = ptx::pack_bf16x2(__uint_as_float(in[g] << 16) * a, __uint_as_float(in[g] & 0xFFFF0000u) * a);
+    reinterpret_cast<uint4*>(gh)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 v = reinterpret_cast<float4*>(gw)[i];
+    v.x *= a; v.y *= a; v.z *= a; v.w *= a;
+    reinterpret_cast<float4*>(gw)[i] = v;
+  }
+}
+
 __global__ void timeout_selftest_kernel(int* hdr, unsigned long long timeout_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x != 0) return;
@@ -283,6 +307,13 @@ cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long 
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl, long long N, int reduce_sum,
                             float* loss, int* n_valid_out, float* row_loss, cudaStream_t s) {
   finalize_kernel<<<1, FIN_THREADS, 0, s>>>(hdr, idx, rl, N, reduce_sum, loss, n_valid_out, row_loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_grads(uint16_t* grad_hidden, long long n_hidden, float* grad_weight, long long n_weight,
+                               const float* scale, cudaStream_t s) {
+  const long long n8 = n_hidden / 8, n4 = n_weight / 4;
+  scale_grads_kernel<<<grid_for(n8 > n4 ? n8 : n4, 256, 152 * 8), 256, 0, s>>>(grad_hidden, n8, grad_weight, n4, scale);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,8 @@ cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long 
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl,
                             long long N, int reduce_sum, float* loss, int* n_valid_out,
                             float* row_loss, cudaStream_t s);
+cudaError_t launch_scale_grads(uint16_t* grad_hidden, long long n_hidden, float* grad_weight,
+                               long long n_weight, const float* scale, cudaStream_t s);
 cudaError_t launch_timeout_selftest(int* hdr, unsigned long long timeout_ns,
                                     cudaStream_t s);
 

@@ -66,6 +66,8 @@ def library() -> ctypes.CDLL:
     lib.flce_selftest_timeout.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]
     lib.flce_status_string.restype = ctypes.c_char_p
+    lib.flce_scale_grads.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+    lib.flce_scale_grads.restype = ctypes.c_int
     lib.flce_profile_begin.argtypes = []
     lib.flce_profile_begin.restype = ctypes.c_int
     lib.flce_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
@@ -187,6 +189,58 @@ def loss(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, igno
         raise FlceError(s, "flce_loss")
     o["workspace"] = workspace
     return o
+
+
+def scale_grads(grad_hidden: torch.Tensor, grad_weight: torch.Tensor, scale: torch.Tensor, stream=None) -> None:
+    """grad_hidden and grad_weight *= scale (a one-element fp32 CUDA tensor), in place, on the device."""
+    if scale.dtype != torch.float32 or scale.numel() != 1 or not scale.is_cuda:
+        raise TypeError("scale must be a one-element float32 CUDA tensor")
+    N, H = grad_hidden.shape
+    V = grad_weight.shape[0]
+    s = library().flce_scale_grads(_ptr(grad_hidden), _ptr(grad_weight), N, H, V, _ptr(scale.contiguous()),
+                                   _stream(stream))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_scale_grads")
+
+
+class _LinearCrossEntropyFn(torch.autograd.Function):
+    """Forward computes the loss and both gradients in one library call; the
+    backward only scales those gradients by the incoming gradient of the loss."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight, targets, ignore_index, reduction):
+        o = fwd_bwd(hidden.contiguous(), weight.contiguous(), targets.contiguous(), ignore_index, reduction)
+        ctx.grads = (o["grad_hidden"], o["grad_weight"])
+        ctx.n_valid = o["n_valid"]
+        return o["loss"].reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        gh, gw = ctx.grads
+        ctx.grads = None
+        scale_grads(gh, gw, grad_loss.detach().reshape(1).to(torch.float32))
+        # autograd casts grad_weight (fp32) to the weight's dtype if they differ
+        return gh, gw, None, None, None
+
+
+def linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                         ignore_index: int = -100, reduction: str = "mean") -> torch.Tensor:
+    """Drop-in for ``F.cross_entropy(hidden @ weight.T, targets, ignore_index=...)``
+    with autograd support; the N x V logits are never materialised."""
+    return _LinearCrossEntropyFn.apply(hidden, weight, targets, ignore_index, reduction)
+
+
+class LinearCrossEntropy(torch.nn.Module):
+    """LM head + cross-entropy as one module: ``loss = module(hidden, targets)``."""
+
+    def __init__(self, weight: torch.Tensor, ignore_index: int = -100, reduction: str = "mean"):
+        super().__init__()
+        self.weight = torch.nn.Parameter(weight)
+        self.ignore_index = ignore_index
+        self.reduction = reduction
+
+    def forward(self, hidden: torch.Tensor, targets: torch.Tensor) -> torch.Tensor:
+        return linear_cross_entropy(hidden, self.weight, targets, self.ignore_index, self.reduction)
 
 
 def query_status(workspace: torch.Tensor, stream=None) -> int:

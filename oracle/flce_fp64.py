@@ -223,3 +223,44 @@ def grad_weight_rows(hidden_bits, weight_bits, targets, lse, vocab_rows,
     P -= (t[valid][:, None] == vr[None, :])
     dZs = P * grad_scale(n_valid, reduction)
     return dZs.T @ Xv
+
+
+# ---------------------------------------------------------------------------
+# Final RMSNorm fused in front of the LM head ("Alisa's book of LLMs",
+# transformer section: final norm, then the unembedding; RMSNorm divides every
+# element of the hidden state by its RMS, then multiplies by a learned
+# per-dimension gain).  Reading taken: eps inside the square root,
+# rms_n = sqrt(mean_h(h_nh^2) + eps).
+# ---------------------------------------------------------------------------
+
+def rmsnorm_rows(Hs: np.ndarray, gain: np.ndarray, eps: float):
+    """x = (h / rms(h)) * gain, with xhat = h / rms(h) and r = 1 / rms(h)."""
+    r = 1.0 / np.sqrt(np.mean(Hs * Hs, axis=1) + eps)
+    xhat = Hs * r[:, None]
+    return xhat * gain[None, :], xhat, r
+
+
+def rmsnorm_backward(dX: np.ndarray, xhat: np.ndarray, r: np.ndarray, gain: np.ndarray):
+    """Chain rule through x = xhat * gain, xhat = h * r, r = (mean(h^2)+eps)^-1/2:
+    dgain = sum_n dX_n * xhat_n;  dh_n = r_n (gain * dX_n - xhat_n * mean(gain * dX_n * xhat_n))."""
+    dgain = (dX * xhat).sum(axis=0)
+    gdx = dX * gain[None, :]
+    dh = r[:, None] * (gdx - xhat * np.mean(gdx * xhat, axis=1, keepdims=True))
+    return dh, dgain
+
+
+def rmsnorm_flce_oracle_f64(Hs: np.ndarray, gain: np.ndarray, W: np.ndarray, targets, eps: float = 1e-6,
+                            ignore_index: int = -100, reduction: str = "mean") -> dict:
+    """loss of the LM head on the normalised hidden states, and the gradients
+    with respect to the un-normalised hidden states, the gain and the weight."""
+    X, xhat, r = rmsnorm_rows(Hs, gain, eps)
+    o = flce_oracle_f64(X, W, targets, ignore_index, reduction)
+    dh, dgain = rmsnorm_backward(o["grad_hidden"], xhat, r, gain)
+    return {"loss": o["loss"], "n_valid": o["n_valid"], "row_loss": o["row_loss"], "normed": X,
+            "grad_hidden": dh, "grad_gain": dgain, "grad_weight": o["grad_weight"]}
+
+
+def rmsnorm_flce_oracle(hidden_bits, gain_bits, weight_bits, targets, eps: float = 1e-6,
+                        ignore_index: int = -100, reduction: str = "mean") -> dict:
+    return rmsnorm_flce_oracle_f64(decode_bf16(hidden_bits), decode_bf16(gain_bits), decode_bf16(weight_bits),
+                                   targets, eps, ignore_index, reduction)
