@@ -138,6 +138,32 @@ flce_status flce_loss(const void* hidden, const void* weight,
                       size_t workspace_bytes, void* stream);
 
 /*
+ * The final RMSNorm fused in front of the LM head ("Alisa's book of LLMs",
+ * transformer section: final norm, then unembedding; RMSNorm divides every
+ * element of the hidden state by its RMS and multiplies by a learned
+ * per-dimension gain).  With h = hidden (pre-norm, bf16 [N,H]) and
+ * g = gain (bf16 [H]):
+ *   x_n = h_n * r_n * g,   r_n = 1 / sqrt(mean_h(h_nh^2) + eps)
+ * then the fused linear cross-entropy of x (rounded to bf16) against weight.
+ * Outputs: loss, n_valid, row_loss as flce_fwd_bwd; grad_hidden (bf16
+ * [N,H]) is the gradient with respect to the PRE-norm hidden states,
+ *   dh_n = r_n (g * dx_n - xhat_n * mean_h(g * dx_n * xhat_n)),  xhat_n = h_n r_n,
+ * grad_gain (fp32 [H]) = sum_n dx_n * xhat_n (summed over chunks in a fixed
+ * order), grad_weight (fp32 [V,H]) as flce_fwd_bwd.  eps >= 0.  Workspace:
+ * flce_rmsnorm_workspace_bytes (the 5% rule plus 4 bytes per chunk row and
+ * per chunk and hidden unit).
+ */
+size_t flce_rmsnorm_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags);
+flce_status flce_rmsnorm_fwd_bwd(const void* hidden, const void* gain, float eps,
+                                 const void* weight, const int32_t* targets,
+                                 int64_t N, int64_t H, int64_t V,
+                                 int32_t ignore_index, uint32_t flags,
+                                 float* loss, int32_t* n_valid, float* row_loss,
+                                 void* grad_hidden, float* grad_gain,
+                                 float* grad_weight, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * grad_hidden (bf16 [N,H]) and grad_weight (fp32 [V,H]) multiplied in place by
  * the fp32 scalar at device address `scale` (read on the device, so the call
  * does not synchronise).  This is the backward of the fused op inside an

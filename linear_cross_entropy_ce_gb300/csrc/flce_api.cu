@@ -89,8 +89,9 @@ struct Plan {
   long long N = 0, H = 0, V = 0, C = 0, ldz = 0, n_chunks = 0;
   int nvt = 0, nparts = 0, splits = 1, kb_per_split = 0;
   long long n_counters = 0, flags_per_chunk = 0;
-  bool fwd_only = false;
-  size_t o_idx = 0, o_rl = 0, o_cnt = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, o_dx = 0, total = 0;
+  bool fwd_only = false, norm = false;
+  size_t o_idx = 0, o_rl = 0, o_cnt = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, o_dx = 0, o_rinv = 0,
+         o_dg = 0, total = 0;
 };
 
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -101,9 +102,9 @@ constexpr int MAX_SPLITS = 8;   // splits are summed one after another: keep the
 
 // Workspace layout for chunks of C rows.  Only the bf16 C x V logits buffer
 // (absent for the forward-only call) grows with V.
-Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_only) {
+Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_only, bool norm = false) {
   Plan p;
-  p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only;
+  p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only; p.norm = norm;
   p.ldz = cdiv(V, 64) * 64;
   p.nvt = static_cast<int>(cdiv(V, BN));
   p.nparts = static_cast<int>(cdiv(V, PART_COLS));
@@ -126,6 +127,10 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
     p.o_z = off; off += al256(size_t(C) * p.ldz * 2);
     if (p.splits > 1) { p.o_dx = off; off += al256(size_t(C) * H * 4); }
   }
+  if (norm) {   // final RMSNorm: 1/rms per chunk row, d(gain) partial per chunk
+    p.o_rinv = off; off += al256(size_t(C) * 4);
+    p.o_dg = off;   off += al256(size_t(p.n_chunks) * H * 4);
+  }
   p.total = off;
   return p;
 }
@@ -146,22 +151,24 @@ int preferred_splits(long long C, long long H, long long V, int pairs) {
 
 long long max_chunk(long long N) { return cdiv(N, BM) * BM; }
 
-Plan plan_for_chunk(long long N, long long H, long long V, long long C, bool fwd_only, int pairs, size_t bytes) {
-  Plan p = layout(N, H, V, C, preferred_splits(C, H, V, pairs), fwd_only);
-  if (p.total > bytes) p = layout(N, H, V, C, 1, fwd_only);
+Plan plan_for_chunk(long long N, long long H, long long V, long long C, bool fwd_only, int pairs, size_t bytes,
+                    bool norm = false) {
+  Plan p = layout(N, H, V, C, preferred_splits(C, H, V, pairs), fwd_only, norm);
+  if (p.total > bytes) p = layout(N, H, V, C, 1, fwd_only, norm);
   return p;
 }
 
 // Largest chunk (multiple of 128 rows) whose plan fits in `bytes`.
-bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, int pairs, Plan* out) {
+bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, int pairs, Plan* out,
+                    bool norm = false) {
   long long lo = BM, hi = max_chunk(N);
-  if (layout(N, H, V, lo, 1, fwd_only).total > bytes) return false;
-  while (lo < hi) {   // the size grows with C: bisect over multiples of 128
+  if (layout(N, H, V, lo, 1, fwd_only, norm).total > bytes) return false;
+  while (lo < hi) {   // the size shrinks as C grows only through the d(gain) partials: bisect on the total
     const long long mid = ((lo / BM + hi / BM + 1) / 2) * BM;
-    if (layout(N, H, V, mid, 1, fwd_only).total <= bytes) lo = mid;
+    if (layout(N, H, V, mid, 1, fwd_only, norm).total <= bytes) lo = mid;
     else hi = mid - BM;
   }
-  *out = plan_for_chunk(N, H, V, lo, fwd_only, pairs, bytes);
+  *out = plan_for_chunk(N, H, V, lo, fwd_only, pairs, bytes, norm);
   return true;
 }
 
@@ -176,13 +183,13 @@ bool sizes_ok(long long N, long long H, long long V) {
   return N >= 1 && H >= 8 && V >= 1 && N < (1ll << 31) && V < (1ll << 31) && H <= (1ll << 20) && H % 8 == 0;
 }
 
-size_t default_bytes(long long N, long long H, long long V, bool fwd_only) {
+size_t default_bytes(long long N, long long H, long long V, bool fwd_only, bool norm = false) {
   if (!sizes_ok(N, H, V)) return 0;
   const size_t budget = size_t(N) * size_t(V) * 2 / 20;   // 5% of the bf16 logits
   const int pairs = device_pairs();
   Plan p;
-  if (plan_for_bytes(N, H, V, fwd_only, budget, pairs, &p)) return p.total;
-  return plan_for_chunk(N, H, V, BM, fwd_only, pairs, ~size_t(0)).total;   // never below one 128-row chunk
+  if (plan_for_bytes(N, H, V, fwd_only, budget, pairs, &p, norm)) return p.total;
+  return plan_for_chunk(N, H, V, BM, fwd_only, pairs, ~size_t(0), norm).total;   // never below one 128-row chunk
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -264,7 +271,10 @@ T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws)
 
 flce_status run(const void* hidden, const void* weight, const int32_t* targets, int64_t N, int64_t H, int64_t V,
                 int32_t ii, uint32_t flags, float* loss, int32_t* n_valid, float* row_loss, void* grad_hidden,
-                float* grad_weight, void* ws, size_t ws_bytes, void* stream, bool fwd_only) {
+                float* grad_weight, void* ws, size_t ws_bytes, void* stream, bool fwd_only,
+                const void* gain = nullptr, float eps = 0.f, float* grad_gain = nullptr) {
+  const bool norm = gain != nullptr;
+  if (norm && (!grad_gain || !aligned16(gain) || !aligned4(grad_gain) || !(eps >= 0.f))) return FLCE_EINVAL;
   if (!hidden || !weight || !targets || !loss || !n_valid || !ws) return FLCE_EINVAL;
   if (!fwd_only && (!grad_hidden || !grad_weight)) return FLCE_EINVAL;
   if (flags & ~FLCE_REDUCE_SUM) return FLCE_EINVAL;
@@ -279,7 +289,7 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   if (device_state(&dev) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
   if (dev.major < 10) return FLCE_EUNSUPPORTED;
   Plan p;
-  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, dev.pairs, &p)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, dev.pairs, &p, norm)) return FLCE_EWORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* hdr = at<int>(ws, 0);
@@ -292,6 +302,8 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   float2* part = at<float2>(ws, p.o_part);
   uint16_t* z = fwd_only ? nullptr : at<uint16_t>(ws, p.o_z);
   float* dxacc = (!fwd_only && p.splits > 1) ? at<float>(ws, p.o_dx) : nullptr;
+  float* rinv = norm ? at<float>(ws, p.o_rinv) : nullptr;
+  float* dgp = norm ? at<float>(ws, p.o_dg) : nullptr;
 
   GemmMaps fm, bm;   // forward (logits) and backward (dX + dW) launches
   std::memset(&fm, 0, sizeof(fm));
@@ -340,7 +352,7 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
       2 * static_cast<int>(std::min<long long>(mt * ht * p.splits + cdiv(V, PAIR_M) * ht, dev.pairs));
 
   auto chk = [](cudaError_t e) { return e == cudaSuccess; };
-  count_launches(2 + (fwd_only ? 0 : 1) + p.n_chunks * 2);   // prep, zero, finalize; gather + lse_dz per chunk
+  count_launches(2 + (fwd_only ? 0 : 1) + p.n_chunks * (norm ? 4 : 2) + (norm ? 1 : 0));
   if (!chk(launch_prep(targets, N, static_cast<int>(V), ii, hdr, idx, n_valid, counters, p.n_counters, st)))
     return FLCE_ECUDA;
   if (!fwd_only &&
@@ -349,8 +361,14 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   for (long long c = 0; c < p.n_chunks; ++c) {
     const long long c0 = c * p.C;
     g.c0 = c0;
-    if (!chk(launch_gather(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H, xc, tc, st)))
+    if (norm) {
+      if (!chk(launch_gather_norm(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H,
+                                  static_cast<const uint16_t*>(gain), eps, xc, tc, rinv, st)))
+        return FLCE_ECUDA;
+    } else if (!chk(launch_gather(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H, xc, tc,
+                                  st))) {
       return FLCE_ECUDA;
+    }
     int* sync = counters + c * (2 + p.flags_per_chunk);
     g.mode = MODE_LOGITS;
     g.counter = sync;
@@ -365,8 +383,13 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
     g.accumulate = c > 0 ? 1 : 0;
     g.first_chunk = c == 0 ? 1 : 0;
     if (!chk(gemm_launch(g, bm, grid_bwd, st))) return FLCE_ECUDA;
+    if (norm && !chk(launch_rmsnorm_bwd(hdr, idx, c0, g.C, g.H, static_cast<const uint16_t*>(hidden),
+                                        static_cast<const uint16_t*>(gain), rinv,
+                                        static_cast<uint16_t*>(grad_hidden), dgp + c * H, st)))
+      return FLCE_ECUDA;
   }
   if (!chk(launch_finalize(hdr, idx, rl, N, reduce_sum, loss, n_valid, row_loss, st))) return FLCE_ECUDA;
+  if (norm && !chk(launch_dgain_reduce(dgp, p.n_chunks, g.H, grad_gain, st))) return FLCE_ECUDA;
   return FLCE_OK;
 }
 
@@ -448,6 +471,21 @@ flce_status flce_query_status(const void* workspace, void* stream) {
   if (word & STATUS_TIMEOUT) return FLCE_ETIMEOUT;
   if (word & STATUS_BADTARGET) return FLCE_EBADTARGET;
   return FLCE_OK;
+}
+
+size_t flce_rmsnorm_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags) {
+  if (flags & ~FLCE_REDUCE_SUM) return 0;
+  return default_bytes(N, H, V, false, true);
+}
+
+flce_status flce_rmsnorm_fwd_bwd(const void* hidden, const void* gain, float eps, const void* weight,
+                                 const int32_t* targets, int64_t N, int64_t H, int64_t V, int32_t ignore_index,
+                                 uint32_t flags, float* loss, int32_t* n_valid, float* row_loss, void* grad_hidden,
+                                 float* grad_gain, float* grad_weight, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (!gain || !grad_gain) return FLCE_EINVAL;
+  return run(hidden, weight, targets, N, H, V, ignore_index, flags, loss, n_valid, row_loss, grad_hidden,
+             grad_weight, workspace, workspace_bytes, stream, false, gain, eps, grad_gain);
 }
 
 flce_status flce_scale_grads(void* grad_hidden, float* grad_weight, int64_t N, int64_t H, int64_t V,

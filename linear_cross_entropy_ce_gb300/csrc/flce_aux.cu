@@ -231,6 +231,140 @@ __global__ void __launch_bounds__(FIN_THREADS)
     for (long long i = threadIdx.x; i < N; i += FIN_THREADS) row_loss[idx[i]] = i < nv ? rl[i] : 0.f;
 }
 
+// ---------------------------------------------------------------------------
+// Final RMSNorm fused in front of the LM head ("Alisa's book of LLMs",
+// transformer section: final norm, then unembedding; RMSNorm divides each
+// element by the RMS of the hidden state and multiplies by a learned gain).
+// x = h * r * g with r = 1 / sqrt(mean(h^2) + eps).
+// ---------------------------------------------------------------------------
+constexpr int NORM_THREADS = 128;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Gather one chunk row and normalise it: Xc = bf16(h * r * g), rinv = r.
+__global__ void __launch_bounds__(NORM_THREADS)
+    gather_norm_kernel(const uint16_t* __restrict__ X, const int* __restrict__ t, const int* hdr,
+                       const int* __restrict__ idx, long long c0, int C, int H, const uint16_t* __restrict__ gain,
+                       float eps, uint16_t* __restrict__ xc, int* __restrict__ tc, float* __restrict__ rinv) {
+  __shared__ float red[NORM_THREADS / 32];
+  const int r = blockIdx.x;
+  const int Cl = chunk_rows(hdr, c0, C);
+  if (r >= round_up_rows(Cl, C)) return;
+  uint4* dst = reinterpret_cast<uint4*>(xc + static_cast<size_t>(r) * H);
+  const int n16 = H / 8;
+  if (r >= Cl) {
+    for (int c = threadIdx.x; c < n16; c += NORM_THREADS) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) { tc[r] = -1; rinv[r] = 0.f; }
+    return;
+  }
+  const long long row = idx[c0 + r];
+  const uint4* src = reinterpret_cast<const uint4*>(X + row * H);
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < n16; c += NORM_THREADS) {
+    const uint4 w = src[c];
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a = bf16_lo(q[k]), b = bf16_hi(q[k]);
+      ss = fmaf(a, a, fmaf(b, b, ss));
+    }
+  }
+  ss = block_reduce(ss, AddOp(), 0.f, red);
+  const float rr = rsqrtf(ss / static_cast<float>(H) + eps);
+  const uint4* gs = reinterpret_cast<const uint4*>(gain);
+  for (int c = threadIdx.x; c < n16; c += NORM_THREADS) {
+    const uint4 w = src[c], gw = gs[c];
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w}, gq[4] = {gw.x, gw.y, gw.z, gw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      o[k] = ptx::pack_bf16x2(bf16_lo(q[k]) * rr * bf16_lo(gq[k]), bf16_hi(q[k]) * rr * bf16_hi(gq[k]));
+    dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) { tc[r] = t[row]; rinv[r] = rr; }
+}
+
+// d(gain) partial of one chunk, per column, rows summed in a fixed order:
+// part[h] = sum_rows dx[row, h] * xhat[row, h] (dx is the grad_hidden row the
+// backward GEMM just wrote).  One block owns 32 columns.
+constexpr int DG_THREADS = 256;
+__global__ void __launch_bounds__(DG_THREADS)
+    rmsnorm_dgain_kernel(const int* hdr, const int* __restrict__ idx, long long c0, int C, int H,
+                         const uint16_t* __restrict__ X, const float* __restrict__ rinv,
+                         const uint16_t* __restrict__ gh, float* __restrict__ part) {
+  __shared__ float acc[DG_THREADS / 32][32];
+  const int Cl = chunk_rows(hdr, c0, C);
+  const int lane = threadIdx.x % 32, w = threadIdx.x / 32;
+  const int h = blockIdx.x * 32 + lane;
+  float a = 0.f;
+  if (h < H)
+    for (int r = w; r < Cl; r += DG_THREADS / 32) {
+      const long long row = idx[c0 + r];
+      const float dx = __uint_as_float(static_cast<uint32_t>(gh[row * H + h]) << 16);
+      const float x = __uint_as_float(static_cast<uint32_t>(X[row * H + h]) << 16);
+      a = fmaf(dx, x * rinv[r], a);
+    }
+  acc[w][lane] = a;
+  __syncthreads();
+  if (w == 0 && h < H) {
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < DG_THREADS / 32; ++k) s += acc[k][lane];
+    part[h] = s;
+  }
+}
+
+// In place: grad_hidden row = r (g dx - xhat mean(g dx xhat)) (RMSNorm backward).
+__global__ void __launch_bounds__(NORM_THREADS)
+    rmsnorm_bwd_rows_kernel(const int* hdr, const int* __restrict__ idx, long long c0, int C, int H,
+                            const uint16_t* __restrict__ X, const uint16_t* __restrict__ gain,
+                            const float* __restrict__ rinv, uint16_t* __restrict__ gh) {
+  __shared__ float red[NORM_THREADS / 32];
+  const int r = blockIdx.x;
+  const int Cl = chunk_rows(hdr, c0, C);
+  if (r >= Cl) return;
+  const long long row = idx[c0 + r];
+  const float rr = rinv[r];
+  const uint4* xs = reinterpret_cast<const uint4*>(X + row * H);
+  const uint4* gs = reinterpret_cast<const uint4*>(gain);
+  uint4* ds = reinterpret_cast<uint4*>(gh + row * H);
+  const int n16 = H / 8;
+  float dot = 0.f;
+  for (int c = threadIdx.x; c < n16; c += NORM_THREADS) {
+    const uint4 xw = xs[c], gw = gs[c], dw = ds[c];
+    const uint32_t xq[4] = {xw.x, xw.y, xw.z, xw.w}, gq[4] = {gw.x, gw.y, gw.z, gw.w}, dq[4] = {dw.x, dw.y, dw.z, dw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      dot = fmaf(bf16_lo(gq[k]) * bf16_lo(dq[k]), bf16_lo(xq[k]) * rr, dot);
+      dot = fmaf(bf16_hi(gq[k]) * bf16_hi(dq[k]), bf16_hi(xq[k]) * rr, dot);
+    }
+  }
+  const float mean = block_reduce(dot, AddOp(), 0.f, red) / static_cast<float>(H);
+  for (int c = threadIdx.x; c < n16; c += NORM_THREADS) {
+    const uint4 xw = xs[c], gw = gs[c], dw = ds[c];
+    const uint32_t xq[4] = {xw.x, xw.y, xw.z, xw.w}, gq[4] = {gw.x, gw.y, gw.z, gw.w}, dq[4] = {dw.x, dw.y, dw.z, dw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float d0 = rr * (bf16_lo(gq[k]) * bf16_lo(dq[k]) - bf16_lo(xq[k]) * rr * mean);
+      const float d1 = rr * (bf16_hi(gq[k]) * bf16_hi(dq[k]) - bf16_hi(xq[k]) * rr * mean);
+      o[k] = ptx::pack_bf16x2(d0, d1);
+    }
+    ds[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// grad_gain[h] = sum over chunks, in chunk order, of the chunk partials.
+__global__ void dgain_reduce_kernel(const float* __restrict__ part, long long n_chunks, int H,
+                                    float* __restrict__ grad_gain) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= H) return;
+  double s = 0.0;
+  for (long long c = 0; c < n_chunks; ++c) s += part[c * H + h];
+  grad_gain[h] = static_cast<float>(s);
+}
+
 // grad_hidden (bf16) and grad_weight (fp32) times a device scalar, in place:
 // the backward of the fused op when the incoming gradient of the loss is not
 // one ("efficient-llm-anatomy" README: the backward pass only distributes the
@@ -307,6 +441,29 @@ cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long 
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl, long long N, int reduce_sum,
                             float* loss, int* n_valid_out, float* row_loss, cudaStream_t s) {
   finalize_kernel<<<1, FIN_THREADS, 0, s>>>(hdr, idx, rl, N, reduce_sum, loss, n_valid_out, row_loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_norm(const uint16_t* hidden, const int* targets, const int* hdr, const int* idx,
+                               long long c0, int C, int H, const uint16_t* gain, float eps, uint16_t* xc, int* tc,
+                               float* rinv, cudaStream_t s) {
+  gather_norm_kernel<<<C, NORM_THREADS, 0, s>>>(hidden, targets, hdr, idx, c0, C, H, gain, eps, xc, tc, rinv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_bwd(const int* hdr, const int* idx, long long c0, int C, int H, const uint16_t* hidden,
+                               const uint16_t* gain, const float* rinv, uint16_t* grad_hidden, float* dgain_partial,
+                               cudaStream_t s) {
+  rmsnorm_dgain_kernel<<<(H + 31) / 32, DG_THREADS, 0, s>>>(hdr, idx, c0, C, H, hidden, rinv, grad_hidden,
+                                                            dgain_partial);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  rmsnorm_bwd_rows_kernel<<<C, NORM_THREADS, 0, s>>>(hdr, idx, c0, C, H, hidden, gain, rinv, grad_hidden);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dgain_reduce(const float* partials, long long n_chunks, int H, float* grad_gain, cudaStream_t s) {
+  dgain_reduce_kernel<<<(H + 255) / 256, 256, 0, s>>>(partials, n_chunks, H, grad_gain);
   return cudaGetLastError();
 }
 

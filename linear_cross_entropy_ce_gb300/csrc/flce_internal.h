@@ -97,6 +97,15 @@ cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long 
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl,
                             long long N, int reduce_sum, float* loss, int* n_valid_out,
                             float* row_loss, cudaStream_t s);
+// Final RMSNorm fused in front of the LM head.
+cudaError_t launch_gather_norm(const uint16_t* hidden, const int* targets, const int* hdr, const int* idx,
+                               long long c0, int C, int H, const uint16_t* gain, float eps, uint16_t* xc,
+                               int* tc, float* rinv, cudaStream_t s);
+cudaError_t launch_rmsnorm_bwd(const int* hdr, const int* idx, long long c0, int C, int H,
+                               const uint16_t* hidden, const uint16_t* gain, const float* rinv,
+                               uint16_t* grad_hidden, float* dgain_partial, cudaStream_t s);
+cudaError_t launch_dgain_reduce(const float* partials, long long n_chunks, int H, float* grad_gain,
+                                cudaStream_t s);
 cudaError_t launch_scale_grads(uint16_t* grad_hidden, long long n_hidden, float* grad_weight,
                                long long n_weight, const float* scale, cudaStream_t s);
 cudaError_t launch_timeout_selftest(int* hdr, unsigned long long timeout_ns,

@@ -66,6 +66,11 @@ def library() -> ctypes.CDLL:
     lib.flce_selftest_timeout.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]
     lib.flce_status_string.restype = ctypes.c_char_p
+    lib.flce_rmsnorm_workspace_bytes.argtypes = [i64, i64, i64, u32]
+    lib.flce_rmsnorm_workspace_bytes.restype = sz
+    lib.flce_rmsnorm_fwd_bwd.argtypes = [vp, vp, ctypes.c_float, vp, vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, vp,
+                                         vp, vp, sz, vp]
+    lib.flce_rmsnorm_fwd_bwd.restype = ctypes.c_int
     lib.flce_scale_grads.argtypes = [vp, vp, i64, i64, i64, vp, vp]
     lib.flce_scale_grads.restype = ctypes.c_int
     lib.flce_profile_begin.argtypes = []
@@ -165,6 +170,41 @@ def fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, i
                                workspace.numel(), _stream(stream))
     if s != FLCE_OK:
         raise FlceError(s, "flce_fwd_bwd")
+    o["workspace"] = workspace
+    return o
+
+
+def rmsnorm_fwd_bwd(hidden: torch.Tensor, gain: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                    eps: float = 1e-6, ignore_index: int = -100, reduction: str = "mean", *,
+                    workspace: Optional[torch.Tensor] = None, row_loss: bool = False, out: Optional[dict] = None,
+                    stream=None) -> dict:
+    """Final RMSNorm (x = h / rms(h) * gain) fused in front of the LM head loss.
+
+    grad_hidden is the gradient with respect to the pre-norm hidden states;
+    grad_gain (fp32 [H]) and grad_weight (fp32 [V,H]) as the parameters'."""
+    N, H, V = _check_inputs(hidden, weight, targets)
+    if gain.dtype != torch.bfloat16 or gain.shape != (H,) or not gain.is_cuda or not gain.is_contiguous():
+        raise ValueError("gain must be a contiguous bf16 CUDA tensor of shape [H]")
+    dev = hidden.device
+    if workspace is None:
+        nb = library().flce_rmsnorm_workspace_bytes(N, H, V, REDUCE[reduction])
+        if nb == 0:
+            raise FlceError(FLCE_EINVAL, "workspace size")
+        workspace = new_workspace(nb, dev)
+    o = out if out is not None else {}
+    if "loss" not in o:
+        o["loss"] = torch.empty(1, dtype=torch.float32, device=dev)
+        o["n_valid"] = torch.empty(1, dtype=torch.int32, device=dev)
+        o["grad_hidden"] = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        o["grad_gain"] = torch.empty(H, dtype=torch.float32, device=dev)
+        o["grad_weight"] = torch.empty((V, H), dtype=torch.float32, device=dev)
+        o["row_loss"] = torch.empty(N, dtype=torch.float32, device=dev) if row_loss else None
+    s = library().flce_rmsnorm_fwd_bwd(_ptr(hidden), _ptr(gain), float(eps), _ptr(weight), _ptr(targets), N, H, V,
+                                       int(ignore_index), REDUCE[reduction], _ptr(o["loss"]), _ptr(o["n_valid"]),
+                                       _ptr(o.get("row_loss")), _ptr(o["grad_hidden"]), _ptr(o["grad_gain"]),
+                                       _ptr(o["grad_weight"]), _ptr(workspace), workspace.numel(), _stream(stream))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_rmsnorm_fwd_bwd")
     o["workspace"] = workspace
     return o
 
