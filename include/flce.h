@@ -164,6 +164,52 @@ flce_status flce_rmsnorm_fwd_bwd(const void* hidden, const void* gain, float eps
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * Vocabulary-parallel LM head (the weight split by rows over P ranks, as a
+ * column-parallel linear layer; "Alisa's book of LLMs", parallelism sections:
+ * sharded matmul whose output dimension is split, and tensor parallelism).
+ * Rank r holds weight rows [v0, v0 + V_shard) of a V_total-row weight and
+ * the whole batch.  One step:
+ *  1. flce_vocab_shard_stats: per token, over the shard's logits, the max,
+ *     the sum of exp(z - max) and the target logit (0 when the target is not
+ *     in the shard); ignored tokens give 0, 0, 0.
+ *  2. all-reduce MAX of row_max over ranks; flce_vocab_rescale rescales the
+ *     local sums to the global max (the online-softmax merge, "Numerical
+ *     stability and other tricks"); all-reduce SUM of row_sumexp and of
+ *     row_target_logit.
+ *  3. flce_vocab_finish (any rank): lse = max + log(sum), per-token loss
+ *     lse - z_t, loss = mean (or sum) over valid tokens, n_valid.
+ *  4. flce_vocab_shard_bwd with the global lse: the shard's logits are
+ *     computed again chunk by chunk, dz = (exp(z - lse) - onehot) * s, the
+ *     shard's grad_weight (fp32 [V_shard, H], complete) and this shard's fp32
+ *     part of grad_hidden ([N, H]); all-reduce SUM of the parts gives
+ *     grad_hidden.
+ * The collectives are the caller's (e.g. NCCL); all arrays are device
+ * arrays; targets hold ids in [0, V_total).  Workspaces as flce_fwd_bwd
+ * with V = V_shard (flce_vocab_shard_workspace_bytes).
+ */
+size_t flce_vocab_shard_workspace_bytes(int64_t N, int64_t H, int64_t V_shard, uint32_t flags);
+flce_status flce_vocab_shard_stats(const void* hidden, const void* weight_shard,
+                                   const int32_t* targets, int64_t N, int64_t H,
+                                   int64_t V_shard, int64_t v0, int64_t V_total,
+                                   int32_t ignore_index, float* row_max,
+                                   float* row_sumexp, float* row_target_logit,
+                                   int32_t* n_valid, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+flce_status flce_vocab_rescale(const float* row_max_local, const float* row_max_global,
+                               float* row_sumexp, int64_t N, void* stream);
+flce_status flce_vocab_finish(const float* row_max, const float* row_sumexp,
+                              const float* row_target_logit, const int32_t* targets,
+                              int64_t N, int32_t ignore_index, uint32_t flags,
+                              float* lse, float* row_loss, float* loss,
+                              int32_t* n_valid, void* stream);
+flce_status flce_vocab_shard_bwd(const void* hidden, const void* weight_shard,
+                                 const int32_t* targets, int64_t N, int64_t H,
+                                 int64_t V_shard, int64_t v0, int64_t V_total,
+                                 int32_t ignore_index, uint32_t flags, const float* lse,
+                                 float* grad_hidden_partial, float* grad_weight_shard,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * grad_hidden (bf16 [N,H]) and grad_weight (fp32 [V,H]) multiplied in place by
  * the fp32 scalar at device address `scale` (read on the device, so the call
  * does not synchronise).  This is the backward of the fused op inside an

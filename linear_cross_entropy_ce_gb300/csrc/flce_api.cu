@@ -269,29 +269,63 @@ void count_launches(long long n) {
 template <typename T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
-flce_status run(const void* hidden, const void* weight, const int32_t* targets, int64_t N, int64_t H, int64_t V,
-                int32_t ii, uint32_t flags, float* loss, int32_t* n_valid, float* row_loss, void* grad_hidden,
-                float* grad_weight, void* ws, size_t ws_bytes, void* stream, bool fwd_only,
-                const void* gain = nullptr, float eps = 0.f, float* grad_gain = nullptr) {
-  const bool norm = gain != nullptr;
-  if (norm && (!grad_gain || !aligned16(gain) || !aligned4(grad_gain) || !(eps >= 0.f))) return FLCE_EINVAL;
-  if (!hidden || !weight || !targets || !loss || !n_valid || !ws) return FLCE_EINVAL;
-  if (!fwd_only && (!grad_hidden || !grad_weight)) return FLCE_EINVAL;
-  if (flags & ~FLCE_REDUCE_SUM) return FLCE_EINVAL;
-  if (N < 1 || H < 1 || V < 1) return FLCE_EINVAL;
-  if (!sizes_ok(N, H, V)) return FLCE_EUNSUPPORTED;
-  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(ws) || !aligned4(targets) || !aligned4(loss) ||
-      !aligned4(n_valid) || (row_loss && !aligned4(row_loss)))
+// One call of the library: the plain fused op, the forward-only loss, the
+// fused final RMSNorm, or one of the two passes over a vocabulary shard.
+enum JobKind { JOB_FWD_BWD, JOB_LOSS, JOB_SHARD_STATS, JOB_SHARD_BWD };
+
+struct Job {
+  JobKind kind = JOB_FWD_BWD;
+  const void* hidden = nullptr;
+  const void* weight = nullptr;      // the rows the GEMMs see: [V, H] (a shard: rows v0 .. v0+V-1)
+  const int32_t* targets = nullptr;  // ids in the full vocabulary [0, V_total)
+  int64_t N = 0, H = 0, V = 0, V_total = 0, v0 = 0;
+  int32_t ii = -100;
+  uint32_t flags = 0;
+  float* loss = nullptr;
+  int32_t* n_valid = nullptr;
+  float* row_loss = nullptr;
+  void* grad_hidden = nullptr;       // bf16 [N, H], or fp32 when grad_hidden_f32
+  bool grad_hidden_f32 = false;
+  float* grad_weight = nullptr;
+  const void* gain = nullptr;        // final RMSNorm
+  float eps = 0.f;
+  float* grad_gain = nullptr;
+  float* row_max = nullptr;          // shard statistics
+  float* row_sumexp = nullptr;
+  float* row_zt = nullptr;
+  const float* lse = nullptr;        // global log-sum-exp for the shard backward
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  void* stream = nullptr;
+};
+
+flce_status run(const Job& j) {
+  const bool fwd_only = j.kind == JOB_LOSS || j.kind == JOB_SHARD_STATS;
+  const bool norm = j.gain != nullptr;
+  const int64_t N = j.N, H = j.H, V = j.V;
+  if (norm && (!j.grad_gain || !aligned16(j.gain) || !aligned4(j.grad_gain) || !(j.eps >= 0.f))) return FLCE_EINVAL;
+  if (!j.hidden || !j.weight || !j.targets || !j.ws) return FLCE_EINVAL;
+  if ((j.kind == JOB_FWD_BWD || j.kind == JOB_LOSS) && (!j.loss || !j.n_valid)) return FLCE_EINVAL;
+  if (!fwd_only && (!j.grad_hidden || !j.grad_weight)) return FLCE_EINVAL;
+  if (j.kind == JOB_SHARD_STATS && (!j.row_max || !j.row_sumexp || !j.row_zt)) return FLCE_EINVAL;
+  if (j.kind == JOB_SHARD_BWD && !j.lse) return FLCE_EINVAL;
+  if (j.flags & ~FLCE_REDUCE_SUM) return FLCE_EINVAL;
+  if (N < 1 || H < 1 || V < 1 || j.v0 < 0 || j.V_total < j.v0 + V) return FLCE_EINVAL;
+  if (!sizes_ok(N, H, V) || j.V_total >= (1ll << 31)) return FLCE_EUNSUPPORTED;
+  if (!aligned16(j.hidden) || !aligned16(j.weight) || !aligned16(j.ws) || !aligned4(j.targets) ||
+      (j.loss && !aligned4(j.loss)) || (j.n_valid && !aligned4(j.n_valid)) || (j.row_loss && !aligned4(j.row_loss)))
     return FLCE_EUNSUPPORTED;
-  if (!fwd_only && (!aligned16(grad_hidden) || !aligned16(grad_weight))) return FLCE_EUNSUPPORTED;
+  if (!fwd_only && (!aligned16(j.grad_hidden) || !aligned16(j.grad_weight))) return FLCE_EUNSUPPORTED;
+  if (j.lse && !aligned4(j.lse)) return FLCE_EUNSUPPORTED;
 
   DeviceState dev;
   if (device_state(&dev) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
   if (dev.major < 10) return FLCE_EUNSUPPORTED;
   Plan p;
-  if (!plan_for_bytes(N, H, V, fwd_only, ws_bytes, dev.pairs, &p, norm)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, fwd_only, j.ws_bytes, dev.pairs, &p, norm)) return FLCE_EWORKSPACE;
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t st = static_cast<cudaStream_t>(j.stream);
+  void* ws = j.ws;
   int* hdr = at<int>(ws, 0);
   int* idx = at<int>(ws, p.o_idx);
   float* rl = at<float>(ws, p.o_rl);
@@ -309,19 +343,19 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   std::memset(&fm, 0, sizeof(fm));
   std::memset(&bm, 0, sizeof(bm));
   const unsigned long long hb = static_cast<unsigned long long>(H) * 2;
-  bool ok = make_map(&fm.a0, xc, H, p.C, hb, BK, BM) && make_map(&fm.b0, weight, H, V, hb, BK, BN / 2);
+  bool ok = make_map(&fm.a0, xc, H, p.C, hb, BK, BM) && make_map(&fm.b0, j.weight, H, V, hb, BK, BN / 2);
   if (!fwd_only)
-    ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, weight, H, V, hb, 64, BK) &&
+    ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, j.weight, H, V, hb, 64, BK) &&
          make_map(&bm.a1, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&bm.b1, xc, H, p.C, hb, 64, BK) &&
-         make_map(&bm.out, grad_weight, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
+         make_map(&bm.out, j.grad_weight, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         make_map(&bm.pf, grad_weight, H, V, static_cast<unsigned long long>(H) * 4, BN, BM,
+         make_map(&bm.pf, j.grad_weight, H, V, static_cast<unsigned long long>(H) * 4, BN, BM,
                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE) &&
          (!dxacc || make_map(&bm.dx, dxacc, H, p.C, static_cast<unsigned long long>(H) * 4, 16, BM,
                              CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B));
   if (!ok) return FLCE_ECUDA;
 
-  const int reduce_sum = (flags & FLCE_REDUCE_SUM) ? 1 : 0;
+  const int reduce_sum = (j.flags & FLCE_REDUCE_SUM) ? 1 : 0;
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
   g.hdr = hdr;
@@ -339,8 +373,9 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
   g.zt = zt;
   g.tc = tc;
   g.idx = idx;
-  g.grad_hidden = static_cast<uint16_t*>(grad_hidden);
-  g.grad_weight = grad_weight;
+  g.grad_hidden = j.grad_hidden_f32 ? nullptr : static_cast<uint16_t*>(j.grad_hidden);
+  g.grad_hidden_f32 = j.grad_hidden_f32 ? static_cast<float*>(j.grad_hidden) : nullptr;
+  g.grad_weight = j.grad_weight;
   g.splits = p.splits;
   g.kb_per_split = p.kb_per_split;
   g.dxacc = dxacc;
@@ -352,29 +387,40 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
       2 * static_cast<int>(std::min<long long>(mt * ht * p.splits + cdiv(V, PAIR_M) * ht, dev.pairs));
 
   auto chk = [](cudaError_t e) { return e == cudaSuccess; };
-  count_launches(2 + (fwd_only ? 0 : 1) + p.n_chunks * (norm ? 4 : 2) + (norm ? 1 : 0));
-  if (!chk(launch_prep(targets, N, static_cast<int>(V), ii, hdr, idx, n_valid, counters, p.n_counters, st)))
+  const bool stats = j.kind == JOB_SHARD_STATS;
+  const int v0 = static_cast<int>(j.v0);
+  count_launches(1 + (fwd_only ? 0 : 1) + (j.kind == JOB_SHARD_BWD ? 0 : 1) + p.n_chunks * (norm ? 4 : 2) +
+                 (norm ? 1 : 0));
+  if (!chk(launch_prep(j.targets, N, static_cast<int>(j.V_total), j.ii, hdr, idx, j.n_valid, counters,
+                       p.n_counters, st)))
     return FLCE_ECUDA;
-  if (!fwd_only &&
-      !chk(launch_zero_ignored(hdr, idx, N, static_cast<int>(H), static_cast<uint16_t*>(grad_hidden), st)))
+  if (!fwd_only && !chk(launch_zero_ignored(hdr, idx, N, H * (j.grad_hidden_f32 ? 4 : 2), j.grad_hidden, st)))
+    return FLCE_ECUDA;
+  if (stats && !chk(launch_shard_stats_ignored(hdr, idx, N, j.row_max, j.row_sumexp, j.row_zt, st)))
     return FLCE_ECUDA;
   for (long long c = 0; c < p.n_chunks; ++c) {
     const long long c0 = c * p.C;
     g.c0 = c0;
     if (norm) {
-      if (!chk(launch_gather_norm(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H,
-                                  static_cast<const uint16_t*>(gain), eps, xc, tc, rinv, st)))
+      if (!chk(launch_gather_norm(static_cast<const uint16_t*>(j.hidden), j.targets, hdr, idx, c0, g.C, g.H,
+                                  static_cast<const uint16_t*>(j.gain), j.eps, xc, tc, rinv, st)))
         return FLCE_ECUDA;
-    } else if (!chk(launch_gather(static_cast<const uint16_t*>(hidden), targets, hdr, idx, c0, g.C, g.H, xc, tc,
-                                  st))) {
+    } else if (!chk(launch_gather(static_cast<const uint16_t*>(j.hidden), j.targets, hdr, idx, c0, g.C, g.H, xc,
+                                  tc, v0, g.V, st))) {
       return FLCE_ECUDA;
     }
     int* sync = counters + c * (2 + p.flags_per_chunk);
     g.mode = MODE_LOGITS;
     g.counter = sync;
     if (!chk(gemm_launch(g, fm, grid_logits, st))) return FLCE_ECUDA;
+    if (stats) {
+      if (!chk(launch_shard_stats(hdr, idx, c0, g.C, p.nparts, part, zt, tc, j.row_max, j.row_sumexp, j.row_zt,
+                                  st)))
+        return FLCE_ECUDA;
+      continue;
+    }
     if (!chk(launch_lse_dz(hdr, c0, g.C, g.V, p.ldz, p.nparts, part, zt, tc, rl, z, reduce_sum, fwd_only ? 0 : 1,
-                           st)))
+                           j.lse, idx, st)))
       return FLCE_ECUDA;
     if (fwd_only) continue;
     g.mode = MODE_BWD;
@@ -383,14 +429,32 @@ flce_status run(const void* hidden, const void* weight, const int32_t* targets, 
     g.accumulate = c > 0 ? 1 : 0;
     g.first_chunk = c == 0 ? 1 : 0;
     if (!chk(gemm_launch(g, bm, grid_bwd, st))) return FLCE_ECUDA;
-    if (norm && !chk(launch_rmsnorm_bwd(hdr, idx, c0, g.C, g.H, static_cast<const uint16_t*>(hidden),
-                                        static_cast<const uint16_t*>(gain), rinv,
-                                        static_cast<uint16_t*>(grad_hidden), dgp + c * H, st)))
+    if (norm && !chk(launch_rmsnorm_bwd(hdr, idx, c0, g.C, g.H, static_cast<const uint16_t*>(j.hidden),
+                                        static_cast<const uint16_t*>(j.gain), rinv,
+                                        static_cast<uint16_t*>(j.grad_hidden), dgp + c * H, st)))
       return FLCE_ECUDA;
   }
-  if (!chk(launch_finalize(hdr, idx, rl, N, reduce_sum, loss, n_valid, row_loss, st))) return FLCE_ECUDA;
-  if (norm && !chk(launch_dgain_reduce(dgp, p.n_chunks, g.H, grad_gain, st))) return FLCE_ECUDA;
+  if (j.kind == JOB_FWD_BWD || j.kind == JOB_LOSS) {
+    if (!chk(launch_finalize(hdr, idx, rl, N, reduce_sum, j.loss, j.n_valid, j.row_loss, st))) return FLCE_ECUDA;
+  }
+  if (norm && !chk(launch_dgain_reduce(dgp, p.n_chunks, g.H, j.grad_gain, st))) return FLCE_ECUDA;
   return FLCE_OK;
+}
+
+flce_status run(const void* hidden, const void* weight, const int32_t* targets, int64_t N, int64_t H, int64_t V,
+                int32_t ii, uint32_t flags, float* loss, int32_t* n_valid, float* row_loss, void* grad_hidden,
+                float* grad_weight, void* ws, size_t ws_bytes, void* stream, bool fwd_only,
+                const void* gain = nullptr, float eps = 0.f, float* grad_gain = nullptr) {
+  Job j;
+  j.kind = fwd_only ? JOB_LOSS : JOB_FWD_BWD;
+  j.hidden = hidden; j.weight = weight; j.targets = targets;
+  j.N = N; j.H = H; j.V = V; j.V_total = V; j.v0 = 0;
+  j.ii = ii; j.flags = flags;
+  j.loss = loss; j.n_valid = n_valid; j.row_loss = row_loss;
+  j.grad_hidden = grad_hidden; j.grad_weight = grad_weight;
+  j.gain = gain; j.eps = eps; j.grad_gain = grad_gain;
+  j.ws = ws; j.ws_bytes = ws_bytes; j.stream = stream;
+  return run(j);
 }
 
 }  // namespace
@@ -486,6 +550,66 @@ flce_status flce_rmsnorm_fwd_bwd(const void* hidden, const void* gain, float eps
   if (!gain || !grad_gain) return FLCE_EINVAL;
   return run(hidden, weight, targets, N, H, V, ignore_index, flags, loss, n_valid, row_loss, grad_hidden,
              grad_weight, workspace, workspace_bytes, stream, false, gain, eps, grad_gain);
+}
+
+size_t flce_vocab_shard_workspace_bytes(int64_t N, int64_t H, int64_t V_shard, uint32_t flags) {
+  if (flags & ~FLCE_REDUCE_SUM) return 0;
+  return default_bytes(N, H, V_shard, false);
+}
+
+flce_status flce_vocab_shard_stats(const void* hidden, const void* weight_shard, const int32_t* targets, int64_t N,
+                                   int64_t H, int64_t V_shard, int64_t v0, int64_t V_total, int32_t ignore_index,
+                                   float* row_max, float* row_sumexp, float* row_target_logit, int32_t* n_valid,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  Job j;
+  j.kind = JOB_SHARD_STATS;
+  j.hidden = hidden; j.weight = weight_shard; j.targets = targets;
+  j.N = N; j.H = H; j.V = V_shard; j.V_total = V_total; j.v0 = v0; j.ii = ignore_index;
+  j.n_valid = n_valid;
+  j.row_max = row_max; j.row_sumexp = row_sumexp; j.row_zt = row_target_logit;
+  j.ws = workspace; j.ws_bytes = workspace_bytes; j.stream = stream;
+  if (!row_max || !row_sumexp || !row_target_logit || !aligned4(row_max) || !aligned4(row_sumexp) ||
+      !aligned4(row_target_logit))
+    return FLCE_EINVAL;
+  return run(j);
+}
+
+flce_status flce_vocab_rescale(const float* row_max_local, const float* row_max_global, float* row_sumexp,
+                               int64_t N, void* stream) {
+  if (!row_max_local || !row_max_global || !row_sumexp || N < 1) return FLCE_EINVAL;
+  count_launches(1);
+  return launch_vocab_rescale(row_max_local, row_max_global, row_sumexp, N, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FLCE_OK
+             : FLCE_ECUDA;
+}
+
+flce_status flce_vocab_finish(const float* row_max, const float* row_sumexp, const float* row_target_logit,
+                              const int32_t* targets, int64_t N, int32_t ignore_index, uint32_t flags, float* lse,
+                              float* row_loss, float* loss, int32_t* n_valid, void* stream) {
+  if (!row_max || !row_sumexp || !row_target_logit || !targets || !loss || N < 1 || (flags & ~FLCE_REDUCE_SUM))
+    return FLCE_EINVAL;
+  count_launches(1);
+  return launch_vocab_finish(row_max, row_sumexp, row_target_logit, targets, N, ignore_index,
+                             (flags & FLCE_REDUCE_SUM) ? 1 : 0, lse, row_loss, loss, n_valid,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FLCE_OK
+             : FLCE_ECUDA;
+}
+
+flce_status flce_vocab_shard_bwd(const void* hidden, const void* weight_shard, const int32_t* targets, int64_t N,
+                                 int64_t H, int64_t V_shard, int64_t v0, int64_t V_total, int32_t ignore_index,
+                                 uint32_t flags, const float* lse, float* grad_hidden_partial,
+                                 float* grad_weight_shard, void* workspace, size_t workspace_bytes, void* stream) {
+  Job j;
+  j.kind = JOB_SHARD_BWD;
+  j.hidden = hidden; j.weight = weight_shard; j.targets = targets;
+  j.N = N; j.H = H; j.V = V_shard; j.V_total = V_total; j.v0 = v0; j.ii = ignore_index; j.flags = flags;
+  j.lse = lse;
+  j.grad_hidden = grad_hidden_partial; j.grad_hidden_f32 = true;
+  j.grad_weight = grad_weight_shard;
+  j.ws = workspace; j.ws_bytes = workspace_bytes; j.stream = stream;
+  return run(j);
 }
 
 flce_status flce_scale_grads(void* grad_hidden, float* grad_weight, int64_t N, int64_t H, int64_t V,

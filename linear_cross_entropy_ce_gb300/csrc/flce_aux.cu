@@ -111,22 +111,25 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restric
   }
 }
 
-__global__ void zero_ignored_kernel(const int* hdr, const int* __restrict__ idx, long long N, int H,
-                                    uint16_t* __restrict__ gh) {
+// rows of ignored tokens = +0.0; row_bytes = H * element size (16-byte multiple)
+__global__ void zero_ignored_kernel(const int* hdr, const int* __restrict__ idx, long long N, long long row_bytes,
+                                    unsigned char* __restrict__ gh) {
   const long long nv = hdr[HDR_NVALID];
-  const long long per_row = H / 8;
+  const long long per_row = row_bytes / 16;
   const long long total = (N - nv) * per_row;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long r = i / per_row, c = i - r * per_row;
     const long long row = idx[nv + r];
-    reinterpret_cast<uint4*>(gh + row * H)[c] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(gh + row * row_bytes)[c] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
+// tc holds the target relative to the first vocabulary row v0 of the weight
+// the GEMMs see (a vocabulary shard), or -1 when it lies outside [0, vs).
 __global__ void gather_kernel(const uint16_t* __restrict__ X, const int* __restrict__ t, const int* hdr,
                               const int* __restrict__ idx, long long c0, int C, int H,
-                              uint16_t* __restrict__ xc, int* __restrict__ tc) {
+                              uint16_t* __restrict__ xc, int* __restrict__ tc, int v0, int vs) {
   const int r = blockIdx.x;
   const int Cl = chunk_rows(hdr, c0, C);
   if (r >= round_up_rows(Cl, C)) return;
@@ -136,7 +139,10 @@ __global__ void gather_kernel(const uint16_t* __restrict__ X, const int* __restr
     const long long row = idx[c0 + r];
     const uint4* src = reinterpret_cast<const uint4*>(X + row * H);
     for (int c = threadIdx.x; c < n16; c += blockDim.x) dst[c] = src[c];
-    if (threadIdx.x == 0) tc[r] = t[row];
+    if (threadIdx.x == 0) {
+      const int local = t[row] - v0;
+      tc[r] = (local >= 0 && local < vs) ? local : -1;
+    }
   } else {
     for (int c = threadIdx.x; c < n16; c += blockDim.x) dst[c] = make_uint4(0u, 0u, 0u, 0u);
     if (threadIdx.x == 0) tc[r] = -1;
@@ -148,7 +154,8 @@ constexpr int LSE_THREADS = 256;
 __global__ void __launch_bounds__(LSE_THREADS)
     lse_dz_kernel(const int* hdr, long long c0, int C, int V, long long ldz, int nparts,
                   const float2* __restrict__ part, const float* __restrict__ zt, const int* __restrict__ tc,
-                  float* __restrict__ rl, uint16_t* __restrict__ z, int reduce_sum, int make_dz) {
+                  float* __restrict__ rl, uint16_t* __restrict__ z, int reduce_sum, int make_dz,
+                  const float* __restrict__ lse_ext, const int* __restrict__ idx) {
   __shared__ float red[LSE_THREADS / 32];
   const int r = blockIdx.x;
   const int Cl = chunk_rows(hdr, c0, C);
@@ -163,14 +170,20 @@ __global__ void __launch_bounds__(LSE_THREADS)
     return;
   }
   const float2* pr = part + static_cast<size_t>(r) * nparts;
-  float m = -INFINITY;
-  for (int j = tid; j < nparts; j += LSE_THREADS) m = fmaxf(m, pr[j].x);
-  m = block_reduce(m, MaxOp(), -INFINITY, red);
-  float d = 0.f;
-  for (int j = tid; j < nparts; j += LSE_THREADS) d += pr[j].y * exp2f((pr[j].x - m) * LOG2E);
-  d = block_reduce(d, AddOp(), 0.f, red);
-  const float lse = m + logf(d);
-  if (tid == 0) rl[c0 + r] = lse - zt[r];
+  float lse;
+  if (lse_ext) {
+    // vocabulary shard: the log-sum-exp over the whole vocabulary is given
+    lse = lse_ext[idx[c0 + r]];
+  } else {
+    float m = -INFINITY;
+    for (int j = tid; j < nparts; j += LSE_THREADS) m = fmaxf(m, pr[j].x);
+    m = block_reduce(m, MaxOp(), -INFINITY, red);
+    float d = 0.f;
+    for (int j = tid; j < nparts; j += LSE_THREADS) d += pr[j].y * exp2f((pr[j].x - m) * LOG2E);
+    d = block_reduce(d, AddOp(), 0.f, red);
+    lse = m + logf(d);
+    if (tid == 0) rl[c0 + r] = lse - zt[r];
+  }
   if (!make_dz) return;
 
   const long long nv = hdr[HDR_NVALID];
@@ -365,6 +378,85 @@ __global__ void dgain_reduce_kernel(const float* __restrict__ part, long long n_
   grad_gain[h] = static_cast<float>(s);
 }
 
+// ---------------------------------------------------------------------------
+// Vocabulary-parallel LM head: per-token statistics of one vocabulary shard,
+// and the merge of all shards' statistics into the log-sum-exp (the online
+// softmax merge of "Alisa's book of LLMs", applied across shards).
+// ---------------------------------------------------------------------------
+
+// One chunk row: max and sum exp over the shard's parts, and the target logit
+// when the target lies in the shard (else 0), written at the token's row.
+__global__ void __launch_bounds__(LSE_THREADS)
+    shard_stats_kernel(const int* hdr, const int* __restrict__ idx, long long c0, int C, int nparts,
+                       const float2* __restrict__ part, const float* __restrict__ zt, const int* __restrict__ tc,
+                       float* __restrict__ row_max, float* __restrict__ row_sumexp, float* __restrict__ row_zt) {
+  __shared__ float red[LSE_THREADS / 32];
+  const int r = blockIdx.x;
+  const int Cl = chunk_rows(hdr, c0, C);
+  if (r >= Cl) return;
+  const float2* pr = part + static_cast<size_t>(r) * nparts;
+  float m = -INFINITY;
+  for (int j = threadIdx.x; j < nparts; j += LSE_THREADS) m = fmaxf(m, pr[j].x);
+  m = block_reduce(m, MaxOp(), -INFINITY, red);
+  float d = 0.f;
+  for (int j = threadIdx.x; j < nparts; j += LSE_THREADS) d += pr[j].y * exp2f((pr[j].x - m) * LOG2E);
+  d = block_reduce(d, AddOp(), 0.f, red);
+  if (threadIdx.x == 0) {
+    const long long row = idx[c0 + r];
+    row_max[row] = m;
+    row_sumexp[row] = d;
+    row_zt[row] = tc[r] >= 0 ? zt[r] : 0.f;
+  }
+}
+
+// Rows of ignored tokens: max 0, sum 0, target logit 0.
+__global__ void shard_stats_ignored_kernel(const int* hdr, const int* __restrict__ idx, long long N,
+                                           float* row_max, float* row_sumexp, float* row_zt) {
+  const long long nv = hdr[HDR_NVALID];
+  for (long long i = nv + static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < N;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = idx[i];
+    row_max[row] = 0.f;
+    row_sumexp[row] = 0.f;
+    row_zt[row] = 0.f;
+  }
+}
+
+// sum exp of a shard rescaled to the global max: d *= exp(m_local - m_global)
+__global__ void vocab_rescale_kernel(const float* __restrict__ m_local, const float* __restrict__ m_global,
+                                     float* __restrict__ sumexp, long long N) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < N;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    sumexp[i] *= exp2f((m_local[i] - m_global[i]) * LOG2E);
+}
+
+// lse = m + log(sum), row loss = lse - z_t, loss = fixed-order sum / n_valid.
+constexpr int VF_THREADS = 1024;
+__global__ void __launch_bounds__(VF_THREADS)
+    vocab_finish_kernel(const float* __restrict__ m, const float* __restrict__ sumexp, const float* __restrict__ zt,
+                        const int* __restrict__ t, long long N, int ii, int reduce_sum, float* __restrict__ lse,
+                        float* __restrict__ row_loss, float* loss, int* n_valid) {
+  __shared__ double red[VF_THREADS / 32];
+  __shared__ int redn[VF_THREADS / 32];
+  double s = 0.0;
+  int n = 0;
+  for (long long i = threadIdx.x; i < N; i += VF_THREADS) {
+    const bool valid = t[i] != ii;
+    const float l = valid ? m[i] + logf(sumexp[i]) : 0.f;
+    const float rl = valid ? l - zt[i] : 0.f;
+    if (lse) lse[i] = l;
+    if (row_loss) row_loss[i] = rl;
+    s += rl;
+    n += valid ? 1 : 0;
+  }
+  s = block_reduce(s, AddOp(), 0.0, red);
+  n = block_reduce(n, AddOp(), 0, redn);
+  if (threadIdx.x == 0) {
+    *loss = n == 0 ? 0.f : static_cast<float>(reduce_sum ? s : s / static_cast<double>(n));
+    if (n_valid) *n_valid = n;
+  }
+}
+
 // grad_hidden (bf16) and grad_weight (fp32) times a device scalar, in place:
 // the backward of the fused op when the incoming gradient of the loss is not
 // one ("efficient-llm-anatomy" README: the backward pass only distributes the
@@ -419,22 +511,24 @@ cudaError_t launch_prep(const int* targets, long long N, int V, int ii, int* hdr
   return cudaGetLastError();
 }
 
-cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, int H, uint16_t* gh,
+cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, long long row_bytes, void* gh,
                                 cudaStream_t s) {
-  zero_ignored_kernel<<<grid_for(N * (H / 8), 256, 1216), 256, 0, s>>>(hdr, idx, N, H, gh);
+  zero_ignored_kernel<<<grid_for(N * (row_bytes / 16), 256, 1216), 256, 0, s>>>(hdr, idx, N, row_bytes,
+                                                                                static_cast<unsigned char*>(gh));
   return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const uint16_t* hidden, const int* targets, const int* hdr, const int* idx,
-                          long long c0, int C, int H, uint16_t* xc, int* tc, cudaStream_t s) {
-  gather_kernel<<<C, 128, 0, s>>>(hidden, targets, hdr, idx, c0, C, H, xc, tc);
+                          long long c0, int C, int H, uint16_t* xc, int* tc, int v0, int vs, cudaStream_t s) {
+  gather_kernel<<<C, 128, 0, s>>>(hidden, targets, hdr, idx, c0, C, H, xc, tc, v0, vs);
   return cudaGetLastError();
 }
 
 cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long ldz, int nparts,
                           const float2* part, const float* zt, const int* tc, float* rl, uint16_t* z,
-                          int reduce_sum, int make_dz, cudaStream_t s) {
-  lse_dz_kernel<<<C, LSE_THREADS, 0, s>>>(hdr, c0, C, V, ldz, nparts, part, zt, tc, rl, z, reduce_sum, make_dz);
+                          int reduce_sum, int make_dz, const float* lse_ext, const int* idx, cudaStream_t s) {
+  lse_dz_kernel<<<C, LSE_THREADS, 0, s>>>(hdr, c0, C, V, ldz, nparts, part, zt, tc, rl, z, reduce_sum, make_dz,
+                                          lse_ext, idx);
   return cudaGetLastError();
 }
 
@@ -464,6 +558,32 @@ cudaError_t launch_rmsnorm_bwd(const int* hdr, const int* idx, long long c0, int
 
 cudaError_t launch_dgain_reduce(const float* partials, long long n_chunks, int H, float* grad_gain, cudaStream_t s) {
   dgain_reduce_kernel<<<(H + 255) / 256, 256, 0, s>>>(partials, n_chunks, H, grad_gain);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_stats(const int* hdr, const int* idx, long long c0, int C, int nparts, const float2* part,
+                               const float* zt, const int* tc, float* row_max, float* row_sumexp, float* row_zt,
+                               cudaStream_t s) {
+  shard_stats_kernel<<<C, LSE_THREADS, 0, s>>>(hdr, idx, c0, C, nparts, part, zt, tc, row_max, row_sumexp, row_zt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_stats_ignored(const int* hdr, const int* idx, long long N, float* row_max,
+                                       float* row_sumexp, float* row_zt, cudaStream_t s) {
+  shard_stats_ignored_kernel<<<grid_for(N, 256, 1216), 256, 0, s>>>(hdr, idx, N, row_max, row_sumexp, row_zt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vocab_rescale(const float* m_local, const float* m_global, float* sumexp, long long N,
+                                 cudaStream_t s) {
+  vocab_rescale_kernel<<<grid_for(N, 256, 1216), 256, 0, s>>>(m_local, m_global, sumexp, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vocab_finish(const float* m, const float* sumexp, const float* zt, const int* t, long long N,
+                                int ii, int reduce_sum, float* lse, float* row_loss, float* loss, int* n_valid,
+                                cudaStream_t s) {
+  vocab_finish_kernel<<<1, VF_THREADS, 0, s>>>(m, sumexp, zt, t, N, ii, reduce_sum, lse, row_loss, loss, n_valid);
   return cudaGetLastError();
 }
 

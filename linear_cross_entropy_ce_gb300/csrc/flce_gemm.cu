@@ -265,6 +265,13 @@ __device__ __forceinline__ void store_bf16_row(uint16_t* dst, const float* v, in
   }
 }
 
+__device__ __forceinline__ void store_f32_row(float* dst, const float* v, int h, int H) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+    if (h + g * 4 < H)
+      *reinterpret_cast<float4*>(dst + 4 * g) = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+}
+
 __device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s, const Unit& t, int row0, int col0,
                                               uint32_t tbase, int r) {
   const int grow = row0 + r;
@@ -276,7 +283,9 @@ __device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s,
     if (h >= a.H) break;  // warp-uniform
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
-    if (rv) store_bf16_row(a.grad_hidden + tok * a.H + h, v, h, a.H);
+    if (!rv) continue;
+    if (a.grad_hidden_f32) store_f32_row(a.grad_hidden_f32 + tok * a.H + h, v, h, a.H);
+    else store_bf16_row(a.grad_hidden + tok * a.H + h, v, h, a.H);
   }
 }
 
@@ -357,7 +366,8 @@ __device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* 
             v[4 * g] = v[4 * g + 1] = v[4 * g + 2] = v[4 * g + 3] = 0.f;
           }
         }
-        store_bf16_row(a.grad_hidden + tok * a.H + h, v, h, a.H);
+        if (a.grad_hidden_f32) store_f32_row(a.grad_hidden_f32 + tok * a.H + h, v, h, a.H);
+        else store_bf16_row(a.grad_hidden + tok * a.H + h, v, h, a.H);
       }
     }
   }

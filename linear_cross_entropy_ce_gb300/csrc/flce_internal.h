@@ -63,6 +63,7 @@ struct GemmArgs {
   const int* tc;        // [C] chunk targets (-1 for padding rows)
   const int* idx;       // [N] compacted row -> token row
   uint16_t* grad_hidden;// [N][H] bf16
+  float* grad_hidden_f32; // [N][H] fp32 instead of grad_hidden when not null (vocabulary shards)
   float* grad_weight;   // [V][H] fp32 (zero fill of an empty first chunk)
   const float* dxacc;   // [C][H] fp32 sum of the grad_hidden splits (splits > 1)
 };
@@ -85,15 +86,15 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps& m, int grid, cudaStre
 cudaError_t launch_prep(const int* targets, long long N, int V, int ignore_index,
                         int* hdr, int* idx, int* n_valid_out, int* counters, long long n_counters,
                         cudaStream_t s);
-cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, int H,
-                                uint16_t* grad_hidden, cudaStream_t s);
+cudaError_t launch_zero_ignored(const int* hdr, const int* idx, long long N, long long row_bytes,
+                                void* grad_hidden, cudaStream_t s);
 cudaError_t launch_gather(const uint16_t* hidden, const int* targets, const int* hdr,
                           const int* idx, long long c0, int C, int H,
-                          uint16_t* xc, int* tc, cudaStream_t s);
+                          uint16_t* xc, int* tc, int v0, int vs, cudaStream_t s);
 cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long ldz,
                           int nparts, const float2* part, const float* zt, const int* tc,
                           float* rl, uint16_t* z, int reduce_sum, int make_dz,
-                          cudaStream_t s);
+                          const float* lse_ext, const int* idx, cudaStream_t s);
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl,
                             long long N, int reduce_sum, float* loss, int* n_valid_out,
                             float* row_loss, cudaStream_t s);
@@ -105,6 +106,17 @@ cudaError_t launch_rmsnorm_bwd(const int* hdr, const int* idx, long long c0, int
                                const uint16_t* hidden, const uint16_t* gain, const float* rinv,
                                uint16_t* grad_hidden, float* dgain_partial, cudaStream_t s);
 cudaError_t launch_dgain_reduce(const float* partials, long long n_chunks, int H, float* grad_gain,
+                                cudaStream_t s);
+// Vocabulary-parallel LM head.
+cudaError_t launch_shard_stats(const int* hdr, const int* idx, long long c0, int C, int nparts,
+                               const float2* part, const float* zt, const int* tc, float* row_max,
+                               float* row_sumexp, float* row_zt, cudaStream_t s);
+cudaError_t launch_shard_stats_ignored(const int* hdr, const int* idx, long long N, float* row_max,
+                                       float* row_sumexp, float* row_zt, cudaStream_t s);
+cudaError_t launch_vocab_rescale(const float* m_local, const float* m_global, float* sumexp, long long N,
+                                 cudaStream_t s);
+cudaError_t launch_vocab_finish(const float* m, const float* sumexp, const float* zt, const int* t, long long N,
+                                int ii, int reduce_sum, float* lse, float* row_loss, float* loss, int* n_valid,
                                 cudaStream_t s);
 cudaError_t launch_scale_grads(uint16_t* grad_hidden, long long n_hidden, float* grad_weight,
                                long long n_weight, const float* scale, cudaStream_t s);

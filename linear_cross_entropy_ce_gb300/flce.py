@@ -71,6 +71,16 @@ def library() -> ctypes.CDLL:
     lib.flce_rmsnorm_fwd_bwd.argtypes = [vp, vp, ctypes.c_float, vp, vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, vp,
                                          vp, vp, sz, vp]
     lib.flce_rmsnorm_fwd_bwd.restype = ctypes.c_int
+    lib.flce_vocab_shard_workspace_bytes.argtypes = [i64, i64, i64, u32]
+    lib.flce_vocab_shard_workspace_bytes.restype = sz
+    lib.flce_vocab_shard_stats.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_vocab_shard_stats.restype = ctypes.c_int
+    lib.flce_vocab_rescale.argtypes = [vp, vp, vp, i64, vp]
+    lib.flce_vocab_rescale.restype = ctypes.c_int
+    lib.flce_vocab_finish.argtypes = [vp, vp, vp, vp, i64, i32, u32, vp, vp, vp, vp, vp]
+    lib.flce_vocab_finish.restype = ctypes.c_int
+    lib.flce_vocab_shard_bwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, u32, vp, vp, vp, vp, sz, vp]
+    lib.flce_vocab_shard_bwd.restype = ctypes.c_int
     lib.flce_scale_grads.argtypes = [vp, vp, i64, i64, i64, vp, vp]
     lib.flce_scale_grads.restype = ctypes.c_int
     lib.flce_profile_begin.argtypes = []
@@ -227,6 +237,69 @@ def loss(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, igno
                             _ptr(workspace), workspace.numel(), _stream(stream))
     if s != FLCE_OK:
         raise FlceError(s, "flce_loss")
+    o["workspace"] = workspace
+    return o
+
+
+# ---------------------------------------------------------------------------
+# vocabulary-parallel LM head (see include/flce.h); the collectives between
+# the calls are the caller's
+# ---------------------------------------------------------------------------
+
+def _ok(s, what):
+    if s != FLCE_OK:
+        raise FlceError(s, what)
+
+
+def vocab_shard_stats(hidden, weight_shard, targets, v0: int, V_total: int, ignore_index: int = -100,
+                      workspace=None, stream=None) -> dict:
+    N, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    dev = hidden.device
+    if workspace is None:
+        workspace = new_workspace(library().flce_vocab_shard_workspace_bytes(N, H, Vs, 0), dev)
+    o = {k: torch.empty(N, dtype=torch.float32, device=dev) for k in ("row_max", "row_sumexp", "row_target_logit")}
+    o["n_valid"] = torch.empty(1, dtype=torch.int32, device=dev)
+    _ok(library().flce_vocab_shard_stats(_ptr(hidden), _ptr(weight_shard), _ptr(targets), N, H, Vs, v0, V_total,
+                                         int(ignore_index), _ptr(o["row_max"]), _ptr(o["row_sumexp"]),
+                                         _ptr(o["row_target_logit"]), _ptr(o["n_valid"]), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)), "flce_vocab_shard_stats")
+    o["workspace"] = workspace
+    return o
+
+
+def vocab_rescale(row_max_local, row_max_global, row_sumexp, stream=None) -> None:
+    _ok(library().flce_vocab_rescale(_ptr(row_max_local), _ptr(row_max_global), _ptr(row_sumexp),
+                                     row_sumexp.numel(), _stream(stream)), "flce_vocab_rescale")
+
+
+def vocab_finish(row_max, row_sumexp, row_target_logit, targets, ignore_index: int = -100,
+                 reduction: str = "mean", stream=None) -> dict:
+    N = targets.shape[0]
+    dev = targets.device
+    o = {"lse": torch.empty(N, dtype=torch.float32, device=dev),
+         "row_loss": torch.empty(N, dtype=torch.float32, device=dev),
+         "loss": torch.empty(1, dtype=torch.float32, device=dev),
+         "n_valid": torch.empty(1, dtype=torch.int32, device=dev)}
+    _ok(library().flce_vocab_finish(_ptr(row_max), _ptr(row_sumexp), _ptr(row_target_logit), _ptr(targets), N,
+                                    int(ignore_index), REDUCE[reduction], _ptr(o["lse"]), _ptr(o["row_loss"]),
+                                    _ptr(o["loss"]), _ptr(o["n_valid"]), _stream(stream)), "flce_vocab_finish")
+    return o
+
+
+def vocab_shard_bwd(hidden, weight_shard, targets, lse, v0: int, V_total: int, ignore_index: int = -100,
+                    reduction: str = "mean", workspace=None, stream=None) -> dict:
+    N, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    dev = hidden.device
+    if workspace is None:
+        workspace = new_workspace(library().flce_vocab_shard_workspace_bytes(N, H, Vs, REDUCE[reduction]), dev)
+    o = {"grad_hidden_partial": torch.empty((N, H), dtype=torch.float32, device=dev),
+         "grad_weight": torch.empty((Vs, H), dtype=torch.float32, device=dev)}
+    _ok(library().flce_vocab_shard_bwd(_ptr(hidden), _ptr(weight_shard), _ptr(targets), N, H, Vs, v0, V_total,
+                                       int(ignore_index), REDUCE[reduction], _ptr(lse),
+                                       _ptr(o["grad_hidden_partial"]), _ptr(o["grad_weight"]), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)), "flce_vocab_shard_bwd")
     o["workspace"] = workspace
     return o
 
