@@ -54,3 +54,20 @@ def exchange_sums(loss_sum: float, n_valid: int, grad_weight: torch.Tensor):
     scale = 1.0 / n if n else 0.0
     grad_weight.mul_(scale)
     return (t[0].item() * scale, n, scale)
+
+
+def vocab_merge(row_max: torch.Tensor, row_sumexp: torch.Tensor, row_target_logit: torch.Tensor, rescale):
+    """The exchange of the vocabulary-parallel LM head, in place.
+
+    Each rank holds per-token (max, sum of exp(z - max), target logit) over
+    its vocabulary shard.  After the call every rank holds the global max, the
+    sum of exp(z - global max) over the whole vocabulary and the target logit
+    (the online-softmax merge of "Alisa's book of LLMs" applied across ranks).
+    ``rescale(local_max, global_max, sumexp)`` multiplies sumexp by
+    exp(local_max - global_max) in place (``flce.vocab_rescale`` on the GPU).
+    """
+    local_max = row_max.clone()
+    dist.all_reduce(row_max, op=dist.ReduceOp.MAX)
+    rescale(local_max, row_max, row_sumexp)
+    dist.all_reduce(row_sumexp)
+    dist.all_reduce(row_target_logit)

@@ -43,6 +43,55 @@ def _worker(rank, world, port, q):
         dist.destroy_process_group()
 
 
+def _vp_worker(rank, world, port, q):
+    import torch.distributed as dist
+    from linear_cross_entropy_ce_gb300 import workloads as wl
+    from oracle import decode_bf16
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        p = wl.random_problem(40, 16, 101, seed=6, ignore_frac=0.2)
+        bounds = [0, 37, 101]                      # uneven vocabulary shards
+        a, b = bounds[rank], bounds[rank + 1]
+        X = decode_bf16(p["hidden"])
+        W = decode_bf16(p["weight"])[a:b]
+        t = p["targets"].astype(np.int64)
+        z = X @ W.T                                # this rank's logits (fp64)
+        m = torch.from_numpy(z.max(axis=1).copy())
+        d = torch.from_numpy(np.exp(z - z.max(axis=1, keepdims=True)).sum(axis=1))
+        inside = (t >= a) & (t < b)
+        zt = torch.from_numpy(np.where(inside, z[np.arange(40), np.clip(t - a, 0, b - a - 1)], 0.0))
+
+        def rescale(lm, gm, s):
+            s.mul_(torch.exp(lm - gm))
+        fdist.vocab_merge(m, d, zt, rescale)
+        q.put((rank, (m + torch.log(d)).numpy(), zt.numpy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_vocab_merge_matches_oracle():
+    from linear_cross_entropy_ce_gb300 import workloads as wl
+    from oracle import flce_oracle
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_vp_worker, args=(r, 2, port, q)) for r in range(2)]
+    for pr in procs:
+        pr.start()
+    res = [q.get(timeout=180) for _ in range(2)]
+    for pr in procs:
+        pr.join(timeout=60)
+        assert pr.exitcode == 0
+    p = wl.random_problem(40, 16, 101, seed=6, ignore_frac=0.2)
+    full = flce_oracle(p["hidden"], p["weight"], p["targets"])
+    valid = p["targets"] != -100
+    for rank, lse, zt in res:
+        np.testing.assert_allclose(lse[valid], full["lse"][valid], rtol=1e-13)
+        np.testing.assert_allclose((lse - zt)[valid], full["row_loss"][valid], rtol=1e-11, atol=1e-13)
+
+
 def test_shard_rows_partition():
     for N in (1, 7, 203, 4096):
         for world in (1, 2, 3, 8):
