@@ -98,7 +98,8 @@ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 constexpr int DEFAULT_PAIRS = 76;
-constexpr int MAX_SPLITS = 8;   // splits are summed one after another: keep the chain short
+constexpr int MAX_SPLITS = 16;   // splits are summed one after another: keep the chain short
+constexpr int DX_UNIT_KB = 128;  // preferred K blocks of one dX unit
 
 // Workspace layout for chunks of C rows.  Only the bf16 C x V logits buffer
 // (absent for the forward-only call) grows with V.
@@ -135,15 +136,18 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
   return p;
 }
 
-// Vocabulary splits of the grad_hidden GEMM: with dynamic scheduling a dX
-// tile (K = V) should take at most half of a pair's average share of the
-// backward launch, or it alone sets the launch's length.
+// Vocabulary splits of the grad_hidden GEMM.  A dX tile (K = V) should take at
+// most half of a pair's average share of the backward launch, or it alone
+// sets the launch's length; and since the dX units are spread through the dW
+// units (which end the launch), short dX units keep that spread even and the
+// launch's tail short.
 int preferred_splits(long long C, long long H, long long V, int pairs) {
   const double dx_tiles = double(cdiv(C, PAIR_M)) * double(cdiv(H, BN));
   const double unit = double(PAIR_M) * BN * double(V);
   const double work = dx_tiles * unit + double(cdiv(V, PAIR_M)) * double(cdiv(H, BN)) * PAIR_M * BN * double(C);
   const double per_pair = work / double(pairs);
   long long S = static_cast<long long>(std::ceil(unit / (0.5 * per_pair)));
+  S = std::max<long long>(S, cdiv(cdiv(V, BK), DX_UNIT_KB));
   const long long max_by_k = std::max<long long>(1, cdiv(V, BK) / 8);   // >= 8 K blocks per split
   S = std::min<long long>(std::min<long long>(S, MAX_SPLITS), max_by_k);
   return static_cast<int>(std::max<long long>(S, 1));
@@ -378,6 +382,7 @@ flce_status run(const Job& j) {
   g.grad_weight = j.grad_weight;
   g.splits = p.splits;
   g.kb_per_split = p.kb_per_split;
+  g.interleave = 1;
   g.dxacc = dxacc;
 
   // persistent grids: CTA pairs, no more than fit on the device at once

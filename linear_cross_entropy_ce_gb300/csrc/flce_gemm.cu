@@ -4,8 +4,8 @@
 // grad_input and grad_weight from the softmax of those logits).
 //
 //   MODE_LOGITS  z = Xc W^T           A = Xc [C,H] K-major,  B = W [V,H] K-major
-//                epilogue: per row and 256-column vocab tile the tile max m
-//                and sum exp(z - m) (one step of the online softmax of
+//                epilogue: per row and 128-column vocabulary part the part
+//                max m and sum exp(z - m) (one step of the online softmax of
 //                "Alisa's book of LLMs", "Numerical stability and other
 //                tricks"), the target logit, and z - m stored as bf16.
 //   MODE_BWD     the two consumers of dz in one launch:
@@ -18,6 +18,9 @@
 //                epilogue: fp32 tile staged in shared memory and written by a
 //                TMA store (first chunk) or a TMA reduce-add (later chunks),
 //                so the fp32 accumulation happens in L2 in fixed chunk order.
+//                dX units are bound by the tensor cores, dW units by the DRAM
+//                read-modify-write of grad_weight: the claim order spreads
+//                the dX units evenly through the dW units so both run at once.
 //
 // Each tile is 256 x 256 and is computed by a CTA pair (a cluster of two CTAs
 // on two SMs) with tcgen05.mma.cta_group::2: each CTA stages its 128 rows of
@@ -136,8 +139,9 @@ struct Shape {
   int Cl;         // valid rows in this chunk
   int mt, nt;     // LOGITS: pair tiles along M and N; BWD: dX pair tiles along M and N
   int kbt;        // LOGITS: K blocks
-  int n_dx;       // BWD: number of dX units (they come first)
+  int n_dx;       // BWD: number of dX units
   int dw_mt;      // BWD: dW pair tiles along M (vocabulary)
+  int dx_span;    // BWD: the dX units are spread over claim positions [0, dx_span)
   int units;
 };
 
@@ -152,13 +156,24 @@ __device__ __forceinline__ Shape make_shape(const GemmArgs& a) {
     s.kbt = (a.H + BK - 1) / BK;
     s.n_dx = 0;
     s.dw_mt = 0;
+    s.dx_span = 0;
     s.units = s.mt * s.nt;
   } else {
     s.nt = (a.H + BN - 1) / BN;
     s.kbt = 0;
     s.n_dx = s.mt * s.nt * a.splits;
     s.dw_mt = (a.V + PAIR_M - 1) / PAIR_M;
-    s.units = s.Cl > 0 ? s.n_dx + s.dw_mt * s.nt : 0;
+    const int n_dw = s.dw_mt * s.nt;
+    s.units = s.Cl > 0 ? s.n_dx + n_dw : 0;
+    s.dx_span = s.n_dx;   // dX units first
+    if (a.interleave && s.Cl > 0) {
+      // Leave after the last dX unit enough dW units for every other pair to
+      // stay busy while it runs: about one dX unit of work per pair.
+      const long long kb_dw = (s.Cl + BK - 1) / BK;
+      const long long tail =
+          min(static_cast<long long>(n_dw), static_cast<long long>(gridDim.x / 2) * ((a.kb_per_split + kb_dw - 1) / kb_dw));
+      s.dx_span = s.n_dx + n_dw - static_cast<int>(tail);
+    }
   }
   return s;
 }
@@ -173,24 +188,38 @@ struct Unit {
   int kb0, kb1;
 };
 
-// Tile order: LOGITS walks M fastest so the pairs in flight share one W tile;
-// dX and dW walk N fastest so they share one slab of dz.  dX splits come in
-// increasing split order, so every split is claimed after the previous one.
+// Tile order: LOGITS walks M fastest so the pairs in flight share one W tile.
+// BWD: claim position u holds a dX unit when ceil(u n_dx / dx_span) steps up
+// at u (dX units evenly spread over [0, dx_span), the first at u = 0), else
+// the next dW unit.  dX units walk M fastest, so the units claimed close
+// together share one slice of W; then N; then the vocabulary split, so every
+// split is claimed after the previous one of its tile.  dW units walk N
+// fastest so they share one slab of dz.
 __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const Shape& s, int u) {
   Unit t;
   t.split = 0;
   if (a.mode == MODE_LOGITS) {
     const int m = u % s.mt, n = u / s.mt;
     t.kind = U_LOGITS; t.m0 = m * PAIR_M; t.n0 = n * BN; t.ntile = n; t.kb0 = 0; t.kb1 = s.kbt;
-  } else if (u < s.n_dx) {
-    const int n = u % s.nt, rest = u / s.nt;
-    const int m = rest % s.mt, sp = rest / s.mt;
+    return t;
+  }
+  int dx_before = s.n_dx;   // dX units at positions below u
+  bool is_dx = false;
+  if (u < s.dx_span) {
+    const long long span = s.dx_span;
+    dx_before = static_cast<int>((static_cast<long long>(u) * s.n_dx + span - 1) / span);
+    is_dx = static_cast<int>((static_cast<long long>(u + 1) * s.n_dx + span - 1) / span) > dx_before;
+  }
+  if (is_dx) {
+    const int i = dx_before;
+    const int m = i % s.mt, rest = i / s.mt;
+    const int n = rest % s.nt, sp = rest / s.nt;
     const int kbt = (a.V + BK - 1) / BK;
     t.kind = U_DX; t.m0 = m * PAIR_M; t.n0 = n * BN; t.ntile = m * s.nt + n; t.split = sp;
     t.kb0 = sp * a.kb_per_split;
     t.kb1 = min(kbt, t.kb0 + a.kb_per_split);
   } else {
-    const int w = u - s.n_dx;
+    const int w = u - dx_before;
     const int n = w % s.nt, m = w / s.nt;
     t.kind = U_DW; t.m0 = m * PAIR_M; t.n0 = n * BN; t.ntile = n; t.kb0 = 0; t.kb1 = (s.Cl + BK - 1) / BK;
   }

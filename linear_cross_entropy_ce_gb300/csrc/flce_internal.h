@@ -54,6 +54,7 @@ struct GemmArgs {
   int first_chunk;      // BWD: chunk 0 (writes zeros when it is empty)
   int splits;           // BWD: vocabulary splits of the grad_hidden GEMM
   int kb_per_split;     // BWD: K blocks per split
+  int interleave;       // BWD: spread the dX units through the dW units (else dX units first)
   int* flags;           // BWD, splits > 1: per (tile, CTA, warpgroup) count of finished splits (zero before)
   unsigned long long timeout_ns;
   // epilogue operands
