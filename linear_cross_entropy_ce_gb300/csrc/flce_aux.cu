@@ -189,37 +189,43 @@ __global__ void __launch_bounds__(LSE_THREADS)
   const long long nv = hdr[HDR_NVALID];
   const float scale = reduce_sum ? 1.f : 1.f / static_cast<float>(nv);
   const int tgt = tc[r];
-  // four 8-column groups in flight per thread; each group lies in one
-  // 128-column part, where z = stored value + part max
-  constexpr long long STEP = LSE_THREADS * 8LL;
-  for (long long v0 = tid * 8LL; v0 < ldz; v0 += 4 * STEP) {
+  // dz = (exp(z - lse) - [v = t]) * scale, with z = stored value + part max;
+  // four 8-column groups in flight per thread, each inside one 128-column part
+  // (the row length ldz < 2^31, so 32-bit column indices suffice)
+  const int ld = static_cast<int>(ldz);
+  constexpr int STEP = LSE_THREADS * 8;
+  for (int v0 = tid * 8; v0 < ld; v0 += 4 * STEP) {
     uint4 w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const long long v = v0 + q * STEP;
-      w[q] = v < ldz ? *reinterpret_cast<const uint4*>(zr + v) : make_uint4(0u, 0u, 0u, 0u);
+      const int v = v0 + q * STEP;
+      w[q] = v < ld ? __ldcs(reinterpret_cast<const uint4*>(zr + v)) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const long long v = v0 + q * STEP;
-      if (v >= ldz) break;
+      const int v = v0 + q * STEP;
+      if (v >= ld) break;
       uint4 o = make_uint4(0u, 0u, 0u, 0u);
       if (v < V) {
         const float b2 = (pr[v / PART_COLS].x - lse) * LOG2E;
         const uint32_t in[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
-        uint32_t out[4];
+        float d[8];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const float s0 = __uint_as_float(in[g] << 16);
-          const float s1 = __uint_as_float(in[g] & 0xFFFF0000u);
-          const long long c = v + 2 * g;
-          float d0 = (exp2f(fmaf(s0, LOG2E, b2)) - (c == tgt ? 1.f : 0.f)) * scale;
-          float d1 = (exp2f(fmaf(s1, LOG2E, b2)) - (c + 1 == tgt ? 1.f : 0.f)) * scale;
-          if (c >= V) d0 = 0.f;
-          if (c + 1 >= V) d1 = 0.f;
-          out[g] = ptx::pack_bf16x2(d0, d1);
+          d[2 * g] = ptx::ex2(fmaf(__uint_as_float(in[g] << 16), LOG2E, b2));
+          d[2 * g + 1] = ptx::ex2(fmaf(__uint_as_float(in[g] & 0xFFFF0000u), LOG2E, b2));
         }
-        o = make_uint4(out[0], out[1], out[2], out[3]);
+        const unsigned tl = static_cast<unsigned>(tgt - v);
+        if (tl < 8u) {   // the target column is in this group
+#pragma unroll
+          for (int e = 0; e < 8; ++e) d[e] -= (e == static_cast<int>(tl)) ? 1.f : 0.f;
+        }
+        if (v + 8 > V) {   // the group straddles the end of the vocabulary
+#pragma unroll
+          for (int e = 0; e < 8; ++e) if (v + e >= V) d[e] = 0.f;
+        }
+        o = make_uint4(ptx::pack_bf16x2(d[0] * scale, d[1] * scale), ptx::pack_bf16x2(d[2] * scale, d[3] * scale),
+                       ptx::pack_bf16x2(d[4] * scale, d[5] * scale), ptx::pack_bf16x2(d[6] * scale, d[7] * scale));
       }
       *reinterpret_cast<uint4*>(zr + v) = o;
     }

@@ -25,9 +25,9 @@
 // Each tile is 256 x 256 and is computed by a CTA pair (a cluster of two CTAs
 // on two SMs) with tcgen05.mma.cta_group::2: each CTA stages its 128 rows of
 // A and its 128 columns of B (32 KB per K block) and holds 128 accumulator
-// rows in its TMEM.  Per CTA: warp 0 issues TMA loads into a 6-stage ring (in
-// CTA 0 it also claims tiles from a global counter and hands them to both
-// CTAs), warp 1 allocates TMEM and, in CTA 0, one lane issues the MMAs for
+// rows in its TMEM.  Per CTA: warp 0 issues TMA loads into a 6-stage ring (7
+// in the logits launch, whose epilogue needs no staging buffers; in CTA 0 it
+// also claims tiles from a global counter and hands them to both CTAs), warp 1 allocates TMEM and, in CTA 0, one lane issues the MMAs for
 // the pair, warps 2-5 drain two TMEM accumulators (double buffered, 2 x 256
 // columns) so an epilogue overlaps the next tile's main loop.  Every wait is
 // bounded: on time-out a CTA raises an abort flag, lets copies in flight
@@ -39,7 +39,8 @@
 namespace flce {
 namespace {
 
-constexpr int STAGES = 6;
+constexpr int STAGES = 6;                   // TMA ring of the backward launch
+constexpr int STAGES_LOGITS = 7;            // the logits epilogue stages nothing: its ring also takes the staging area
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -60,8 +61,8 @@ constexpr uint16_t PAIR_MASK = 0x3;
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct Ctl {
-  uint64_t full[STAGES];       // CTA 0: both CTAs' loads of a stage landed
-  uint64_t empty[STAGES];      // each CTA: the pair's MMAs released the stage
+  uint64_t full[STAGES_LOGITS];  // CTA 0: both CTAs' loads of a stage landed
+  uint64_t empty[STAGES_LOGITS]; // each CTA: the pair's MMAs released the stage
   uint64_t tfull[2];           // each CTA: accumulator ready
   uint64_t tempty[2];          // CTA 0: both CTAs' epilogues drained the accumulator
   uint64_t sfull[SCHED_SLOTS]; // each CTA: a tile id is in sunit
@@ -75,6 +76,8 @@ struct Ctl {
 constexpr int CTL_BYTES = ((sizeof(Ctl) + 255) / 256) * 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * EPI_GROUPS * STG_BYTES + CTL_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(STAGES_LOGITS * STAGE_BYTES <= STAGES * STAGE_BYTES + 2 * EPI_GROUPS * STG_BYTES,
+              "the extra logits stages fit in the epilogue staging area");
 
 // Readers of a scheduler slot: in CTA 0 the MMA lane and its epilogue
 // threads, in CTA 1 the TMA lane and its epilogue threads.
@@ -257,18 +260,26 @@ __device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, co
   float sum = 0.f;
   uint16_t* zrow = a.z + static_cast<size_t>(grow) * a.ldz + c0;
   const bool store = a.store_z && rv;
+  const float mb = -mx * LOG2E;
 #pragma unroll 1
   for (int j = 0; j < GROUP_COLS / 32; ++j) {
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
     uint32_t pk[16];
+    if (j * 32 + 32 <= ncol) {   // whole block inside the vocabulary
 #pragma unroll
-    for (int k = 0; k < 32; k += 2) {
-      const float s0 = v[k] - mx, s1 = v[k + 1] - mx;
-      const int c = j * 32 + k;
-      if (c < ncol) sum += exp2f(s0 * LOG2E);
-      if (c + 1 < ncol) sum += exp2f(s1 * LOG2E);
-      pk[k / 2] = ptx::pack_bf16x2(s0, s1);
+      for (int k = 0; k < 32; k += 2) {
+        sum += ptx::ex2(fmaf(v[k], LOG2E, mb)) + ptx::ex2(fmaf(v[k + 1], LOG2E, mb));
+        pk[k / 2] = ptx::pack_bf16x2(v[k] - mx, v[k + 1] - mx);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        const int c = j * 32 + k;
+        if (c < ncol) sum += ptx::ex2(fmaf(v[k], LOG2E, mb));
+        if (c + 1 < ncol) sum += ptx::ex2(fmaf(v[k + 1], LOG2E, mb));
+        pk[k / 2] = ptx::pack_bf16x2(v[k] - mx, v[k + 1] - mx);
+      }
     }
     if (store && c0 + j * 32 < a.ldz) {
       uint4* dst = reinterpret_cast<uint4*>(zrow + j * 32);
@@ -428,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (s.units == 0) return;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < STAGES_LOGITS; ++i) {
       ptx::mbar_init(&ctl->full[i], 1);
       ptx::mbar_init(&ctl->empty[i], 1);
     }
@@ -465,6 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const uint64_t to = a.timeout_ns;
   int* hdr = const_cast<int*>(a.hdr);
   const int half = static_cast<int>(rank) * BM;   // this CTA's rows (A) / columns (B) inside a pair tile
+  const uint32_t nstages = a.mode == MODE_LOGITS ? STAGES_LOGITS : STAGES;
 
   if (warp == 0 && lane == 0) {
     // ---------------- (CTA 0: scheduler +) TMA producer ----------------
@@ -525,13 +537,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == nstages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
     }
     if (!ok && lead) {
       // let the copies already in flight land before the pair exits
-      for (int i = 0; i < STAGES; ++i)
+      for (int i = 0; i < nstages; ++i)
         if (issued_mask & (1u << i)) wait_phase(&ctl->full[i], (issued_parity >> i) & 1u, ctl, to, false, hdr, W_DRAIN);
     }
   } else if (warp == 1 && lane == 0 && lead) {
@@ -565,7 +577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           ptx::umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
         }
         ptx::umma_commit_pair(&ctl->empty[stage], PAIR_MASK);   // frees the slot in both CTAs
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == nstages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
       ptx::umma_commit_pair(&ctl->tfull[acc], PAIR_MASK);       // accumulator ready in both CTAs

@@ -290,6 +290,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn_maj
          (static_cast<uint32_t>(m >> 4) << 24);       // M / 16
 }
 
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz:
+// results below the normal range flush to zero, which the softmax sums and the
+// bf16 gradients cannot represent anyway).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
