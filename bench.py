@@ -207,6 +207,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tokens", type=int, default=None, help="override N (small profiling cases)")
     ap.add_argument("--chunk-rows", type=int, default=None, help="override the default 5%% plan")
+    ap.add_argument("--workspace-bytes", type=int, default=None,
+                    help="workspace size to plan for (small profiling cases that keep a full-size plan)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "flce":
         args.warmup = 3
@@ -239,7 +241,7 @@ def main():
     W = torch.from_numpy(p["weight"].view(np.int16)).view(torch.bfloat16).to(dev)
     t = torch.from_numpy(p["targets"]).to(dev)
     nv = int((p["targets"] != -100).sum())
-    ws_bytes = flce.workspace_bytes(N, H, V, chunk_rows=args.chunk_rows)
+    ws_bytes = args.workspace_bytes or flce.workspace_bytes(N, H, V, chunk_rows=args.chunk_rows)
     plan = flce.plan(N, H, V, ws_bytes)
     ws = flce.new_workspace(ws_bytes, dev)
     out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
@@ -328,7 +330,7 @@ def main():
             tj = json.load(open(tpath))
             # only valid for the kernel sources the counters were taken on
             if tj.get("workload") == w.name and tj.get("kernel_sources_sha1") == kernel_sources_sha1() \
-                    and not args.tokens and not args.chunk_rows:
+                    and not args.tokens and not args.chunk_rows and not args.workspace_bytes:
                 traffic = tj.get("dram_bytes_per_launch")
         except Exception:
             traffic = None
