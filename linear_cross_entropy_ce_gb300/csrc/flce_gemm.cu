@@ -120,6 +120,17 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Ctl* ctl
   }
 }
 
+// Wait on a stage barrier of the TMA ring (local, completed by TMA bytes or by
+// the pair's MMA commit).  The common case, a phase that has already
+// completed, costs one CTA-scope try_wait in line; the bounded cluster-scope
+// loop above runs only when the phase is still open.  (Routing every stage
+// wait through that loop cost the logits launch 6-8%.)
+__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, Ctl* ctl, uint64_t timeout_ns, int* hdr,
+                                           int site, int detail) {
+  if (ptx::mbar_test(bar, parity)) return true;
+  return wait_phase(bar, parity, ctl, timeout_ns, true, hdr, site, detail);
+}
+
 // Bounded wait until a global flag reaches `target`.
 __device__ __noinline__ bool wait_flag(const int* flag, int target, Ctl* ctl, uint64_t timeout_ns, int* hdr) {
   if (ptx::ld_acquire_gpu(flag) >= target) return true;
@@ -482,6 +493,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // ---------------- (CTA 0: scheduler +) TMA producer ----------------
     uint32_t stage = 0, phase = 0, sslot = 0, sphase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
+    const uint32_t full0 = ptx::map_to_rank(&ctl->full[0], 0);       // the stage barriers are contiguous
     bool ok = true;
     // CTA 0 claims tiles from the global counter.  After a short tile the
     // claim latency would stall the ring between tiles, so the next tile is
@@ -513,10 +525,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (t.kind == U_DW && a.accumulate) ptx::tma_prefetch_l2_2d(&maps.pf, t.n0, t.m0 + half);
       if (lead && t.kb1 - t.kb0 <= SHORT_TILE_KB) next = atomicAdd(a.counter, 1);
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        if (!wait_phase(&ctl->empty[stage], phase ^ 1u, ctl, to, true, hdr, W_STAGE_EMPTY, u | (stage << 24))) { ok = false; break; }
+        if (!wait_stage(&ctl->empty[stage], phase ^ 1u, ctl, to, hdr, W_STAGE_EMPTY, u | (stage << 24))) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
-        const uint32_t fb = ptx::map_to_rank(&ctl->full[stage], 0);   // CTA 0's barrier
+        const uint32_t fb = full0 + stage * 8u;                        // CTA 0's barrier of this stage
         if (lead) ptx::mbar_arrive_expect_tx(&ctl->full[stage], 2 * STAGE_BYTES);
         const int k0 = kb * BK;
         if (t.kind == U_LOGITS) {
@@ -566,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t d_tmem = tmem + acc * BN;
       bool ok = true;
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        if (!wait_phase(&ctl->full[stage], phase, ctl, to, true, hdr, W_STAGE_FULL, u | (stage << 24))) { ok = false; break; }
+        if (!wait_stage(&ctl->full[stage], phase, ctl, to, hdr, W_STAGE_FULL, u | (stage << 24))) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + stage * STAGE_BYTES);
         const uint32_t sb = sa + A_BYTES;
