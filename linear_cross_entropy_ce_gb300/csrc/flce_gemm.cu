@@ -261,11 +261,18 @@ __device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, co
   for (int j = 0; j < GROUP_COLS / 32; ++j) {
     float v[32];
     ptx::tmem_ld32(tbase + j * 32, v);
+    if (j * 32 + 32 <= ncol) {   // whole block inside the vocabulary
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int c = j * 32 + k;
-      if (c < ncol) mx = fmaxf(mx, v[k]);
-      if (c == tl) ztv = v[k];
+      for (int k = 0; k < 32; ++k) mx = fmaxf(mx, v[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (j * 32 + k < ncol) mx = fmaxf(mx, v[k]);
+    }
+    if (static_cast<unsigned>(tl - j * 32) < 32u) {   // this row's target is in the block
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (j * 32 + k == tl) ztv = v[k];
     }
   }
   float sum = 0.f;
