@@ -138,19 +138,31 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
 
 // Vocabulary splits of the grad_hidden GEMM.  A dX tile (K = V) should take at
 // most half of a pair's average share of the backward launch, or it alone
-// sets the launch's length; and since the dX units are spread through the dW
-// units (which end the launch), short dX units keep that spread even and the
-// launch's tail short.
+// sets the launch's length.  The parts of a tile are summed one after
+// another, each waiting for the previous one to land (a few µs each), so the
+// chain of S parts costs S of those steps unless the dX units are spread
+// through the dW units (the kernel does that when the dW units outnumber what
+// the other pairs need to stay busy during one dX unit).  Spread: short
+// units (~DX_UNIT_KB K blocks) keep the spread even and the launch's tail
+// short.  Not spread: S balances the unit length (kbt / S K blocks of
+// ~0.3 µs) against the chain (S steps of ~4 µs), S ~ sqrt(kbt / 13).
 int preferred_splits(long long C, long long H, long long V, int pairs) {
+  const long long kbt = cdiv(V, BK);
   const double dx_tiles = double(cdiv(C, PAIR_M)) * double(cdiv(H, BN));
   const double unit = double(PAIR_M) * BN * double(V);
   const double work = dx_tiles * unit + double(cdiv(V, PAIR_M)) * double(cdiv(H, BN)) * PAIR_M * BN * double(C);
   const double per_pair = work / double(pairs);
-  long long S = static_cast<long long>(std::ceil(unit / (0.5 * per_pair)));
-  S = std::max<long long>(S, cdiv(cdiv(V, BK), DX_UNIT_KB));
-  const long long max_by_k = std::max<long long>(1, cdiv(V, BK) / 8);   // >= 8 K blocks per split
-  S = std::min<long long>(std::min<long long>(S, MAX_SPLITS), max_by_k);
-  return static_cast<int>(std::max<long long>(S, 1));
+  const long long balance = static_cast<long long>(std::ceil(unit / (0.5 * per_pair)));
+  const long long max_by_k = std::max<long long>(1, kbt / 8);   // >= 8 K blocks per split
+  auto clamp = [&](long long S) {
+    return std::max<long long>(1, std::min<long long>(std::min<long long>(S, MAX_SPLITS), max_by_k));
+  };
+  const long long n_dw = cdiv(V, PAIR_M) * cdiv(H, BN);
+  const long long kb_dw = cdiv(C, BK);
+  const long long spread = clamp(std::max<long long>(balance, cdiv(kbt, DX_UNIT_KB)));
+  if (n_dw > static_cast<long long>(pairs) * cdiv(cdiv(kbt, spread), kb_dw)) return static_cast<int>(spread);
+  const long long chain = std::llround(std::sqrt(double(kbt) / 13.0));
+  return static_cast<int>(clamp(std::min<long long>(balance, chain)));
 }
 
 long long max_chunk(long long N) { return cdiv(N, BM) * BM; }
