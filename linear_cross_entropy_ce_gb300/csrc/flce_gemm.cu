@@ -529,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const Unit t = decode_unit(a, s, u);
       // the epilogue of a dW unit reduce-adds into grad_weight: pull this
       // CTA's 128 x 256 block of it into L2 while the main loop runs
-      if (t.kind == U_DW && a.accumulate) ptx::tma_prefetch_l2_2d(&maps.pf, t.n0, t.m0 + half);
+      if (t.kind == U_DW && a.accumulate && !a.pf_threads) ptx::tma_prefetch_l2_2d(&maps.pf, t.n0, t.m0 + half);
       if (lead && t.kb1 - t.kb0 <= SHORT_TILE_KB) next = atomicAdd(a.counter, 1);
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
         if (!wait_stage(&ctl->empty[stage], phase ^ 1u, ctl, to, hdr, W_STAGE_EMPTY, u | (stage << 24))) { ok = false; break; }
@@ -626,6 +626,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
       const Unit t = decode_unit(a, s, u);
+      if (t.kind == U_DW && a.accumulate && a.pf_threads) {
+        // this thread's row of the grad_weight tile (128 fp32 = 4 lines) into
+        // L2 before the reduce-adds; plain prefetches leave the TMA unit to
+        // the loads, which short grad_weight tiles need
+        const long long vrow = t.m0 + half + r;
+        if (vrow < a.V) {
+          const float* gp = a.grad_weight + vrow * a.H + t.n0 + col0;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            if (t.n0 + col0 + q4 * 32 < a.H) ptx::prefetch_l2(gp + q4 * 32);
+        }
+      }
       ok = wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true, hdr, W_TMEM_FULL, u | (acc << 24));
       if (!ptx::named_bar_and(EPI_BAR_ALL, EPI_THREADS, ok)) break;
       ptx::tc_fence_after();

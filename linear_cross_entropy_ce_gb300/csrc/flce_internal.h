@@ -55,6 +55,8 @@ struct GemmArgs {
   int splits;           // BWD: vocabulary splits of the grad_hidden GEMM
   int kb_per_split;     // BWD: K blocks per split
   int interleave;       // BWD: spread the dX units through the dW units (else dX units first)
+  int pf_threads;       // BWD, accumulating: the epilogue threads prefetch the grad_weight tile into L2
+                        // (else one TMA prefetch when the tile's main loop starts)
   int* flags;           // BWD, splits > 1: per (tile, CTA, warpgroup) count of finished splits (zero before)
   unsigned long long timeout_ns;
   // epilogue operands
