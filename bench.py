@@ -36,12 +36,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 def kernel_sources_sha1() -> str:
+    """Hash of the CUDA sources with comments and blank space removed, so that
+    DRAM counters taken on one build stay attached to it across comment edits."""
     import glob
     import hashlib
+    import re
     h = hashlib.sha1()
     for f in sorted(glob.glob(os.path.join(ROOT, "linear_cross_entropy_ce_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, "r", encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = re.sub(r"\s+", " ", src).strip()
+        h.update(os.path.basename(f).encode() + b"\0" + src.encode())
     return h.hexdigest()
 
 

@@ -5,10 +5,11 @@
 // computes backward during forward": tokens are processed in chunks and each
 // chunk runs all three matmuls).  For chunk c of C valid tokens:
 //   gather   Xc = rows of X for the chunk's valid tokens
-//   LOGITS   z = Xc W^T; per-tile max / sum-exp, target logit, bf16 z - max
+//   LOGITS   z = Xc W^T; per 128-column part max / sum-exp, target logit,
+//            bf16 z - part max
 //   lse_dz   lse per row (fixed-order merge), row loss, dz in place
-//   DX       grad_hidden rows = dz W            (complete per chunk, K = V)
-//   DW       grad_weight (+)= dz^T Xc           (fixed chunk order, fp32)
+//   BWD      one launch: DX grad_hidden rows = dz W (complete per chunk, K = V)
+//            and DW grad_weight (+)= dz^T Xc (fixed chunk order, fp32)
 // The only buffer that scales with V is the C x V bf16 chunk of logits, so
 // the default plan keeps the workspace below 5% of the N x V bf16 logits.
 #include <algorithm>

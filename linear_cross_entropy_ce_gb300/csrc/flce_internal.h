@@ -32,7 +32,7 @@ constexpr int BK = 64;
 constexpr int PART_COLS = 128;
 
 enum GemmMode : int {
-  MODE_LOGITS = 0,  // z = Xc W^T, epilogue: per-tile (max, sum exp), z_t, shifted bf16 logits
+  MODE_LOGITS = 0,  // z = Xc W^T, epilogue: per 128-column part (max, sum exp), z_t, shifted bf16 logits
   MODE_BWD = 1,     // one launch holding both consumers of dz:
                     //   grad_hidden rows = dz W          (units [0, n_dx))
                     //   grad_weight (+)= dz^T Xc         (units [n_dx, n_dx + n_dw))
