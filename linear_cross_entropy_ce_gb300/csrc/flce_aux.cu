@@ -190,44 +190,50 @@ __global__ void __launch_bounds__(LSE_THREADS)
   const float scale = reduce_sum ? 1.f : 1.f / static_cast<float>(nv);
   const int tgt = tc[r];
   // dz = (exp(z - lse) - [v = t]) * scale, with z = stored value + part max;
-  // four 8-column groups in flight per thread, each inside one 128-column part
-  // (the row length ldz < 2^31, so 32-bit column indices suffice)
+  // four 16-column groups (32-byte accesses) in flight per thread, each inside
+  // one 128-column part (the row length ldz < 2^31 is a multiple of 64, so
+  // 32-bit column indices suffice and no group straddles it)
   const int ld = static_cast<int>(ldz);
-  constexpr int STEP = LSE_THREADS * 8;
-  for (int v0 = tid * 8; v0 < ld; v0 += 4 * STEP) {
-    uint4 w[4];
+  constexpr int GW = 16;
+  constexpr int STEP = LSE_THREADS * GW;
+  for (int v0 = tid * GW; v0 < ld; v0 += 4 * STEP) {
+    uint32_t w[4][8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int v = v0 + q * STEP;
-      w[q] = v < ld ? __ldcs(reinterpret_cast<const uint4*>(zr + v)) : make_uint4(0u, 0u, 0u, 0u);
+      if (v < ld) {
+        ptx::ld_global_v8_cs(zr + v, w[q]);
+      } else {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) w[q][g] = 0u;
+      }
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int v = v0 + q * STEP;
       if (v >= ld) break;
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
       if (v < V) {
         const float b2 = (pr[v / PART_COLS].x - lse) * LOG2E;
-        const uint32_t in[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
-        float d[8];
+        float d[GW];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          d[2 * g] = ptx::ex2(fmaf(__uint_as_float(in[g] << 16), LOG2E, b2));
-          d[2 * g + 1] = ptx::ex2(fmaf(__uint_as_float(in[g] & 0xFFFF0000u), LOG2E, b2));
+        for (int g = 0; g < 8; ++g) {
+          d[2 * g] = ptx::ex2(fmaf(__uint_as_float(w[q][g] << 16), LOG2E, b2));
+          d[2 * g + 1] = ptx::ex2(fmaf(__uint_as_float(w[q][g] & 0xFFFF0000u), LOG2E, b2));
         }
         const unsigned tl = static_cast<unsigned>(tgt - v);
-        if (tl < 8u) {   // the target column is in this group
+        if (tl < static_cast<unsigned>(GW)) {   // the target column is in this group
 #pragma unroll
-          for (int e = 0; e < 8; ++e) d[e] -= (e == static_cast<int>(tl)) ? 1.f : 0.f;
+          for (int e = 0; e < GW; ++e) d[e] -= (e == static_cast<int>(tl)) ? 1.f : 0.f;
         }
-        if (v + 8 > V) {   // the group straddles the end of the vocabulary
+        if (v + GW > V) {   // the group straddles the end of the vocabulary
 #pragma unroll
-          for (int e = 0; e < 8; ++e) if (v + e >= V) d[e] = 0.f;
+          for (int e = 0; e < GW; ++e) if (v + e >= V) d[e] = 0.f;
         }
-        o = make_uint4(ptx::pack_bf16x2(d[0] * scale, d[1] * scale), ptx::pack_bf16x2(d[2] * scale, d[3] * scale),
-                       ptx::pack_bf16x2(d[4] * scale, d[5] * scale), ptx::pack_bf16x2(d[6] * scale, d[7] * scale));
+#pragma unroll
+        for (int g = 0; g < 8; ++g) o[g] = ptx::pack_bf16x2(d[2 * g] * scale, d[2 * g + 1] * scale);
       }
-      *reinterpret_cast<uint4*>(zr + v) = o;
+      ptx::st_global_v8(zr + v, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
     }
   }
 }

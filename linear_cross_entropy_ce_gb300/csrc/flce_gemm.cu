@@ -299,10 +299,10 @@ __device__ __forceinline__ void epi_logits(const GemmArgs& a, const Shape& s, co
         pk[k / 2] = ptx::pack_bf16x2(v[k] - mx, v[k + 1] - mx);
       }
     }
-    if (store && c0 + j * 32 < a.ldz) {
-      uint4* dst = reinterpret_cast<uint4*>(zrow + j * 32);
-#pragma unroll
-      for (int g = 0; g < 4; ++g) dst[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+    if (store && c0 + j * 32 < a.ldz) {   // 64 bytes of this row: two 32-byte stores
+      uint16_t* dst = zrow + j * 32;
+      ptx::st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+      ptx::st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
     }
   }
   if (rv) {
