@@ -18,18 +18,22 @@
 //                epilogue: fp32 tile staged in shared memory and written by a
 //                TMA store (first chunk) or a TMA reduce-add (later chunks),
 //                so the fp32 accumulation happens in L2 in fixed chunk order.
-//                dX units are bound by the tensor cores, dW units by the DRAM
-//                read-modify-write of grad_weight: the claim order spreads
-//                the dX units evenly through the dW units so both run at once.
+//                dX units are bound by the tensor cores, dW units (short, 12
+//                K blocks at C = 768) by the latency of their loads under the
+//                grad_weight read-modify-write: where the grad_hidden GEMM is
+//                split, the claim order spreads the dX units evenly through
+//                the dW units so both kinds run at once.
 //
 // Each tile is 256 x 256 and is computed by a CTA pair (a cluster of two CTAs
 // on two SMs) with tcgen05.mma.cta_group::2: each CTA stages its 128 rows of
 // A and its 128 columns of B (32 KB per K block) and holds 128 accumulator
 // rows in its TMEM.  Per CTA: warp 0 issues TMA loads into a 6-stage ring (7
 // in the logits launch, whose epilogue needs no staging buffers; in CTA 0 it
-// also claims tiles from a global counter and hands them to both CTAs), warp 1 allocates TMEM and, in CTA 0, one lane issues the MMAs for
-// the pair, warps 2-5 drain two TMEM accumulators (double buffered, 2 x 256
-// columns) so an epilogue overlaps the next tile's main loop.  Every wait is
+// also claims tiles from a global counter and hands them to both CTAs),
+// warp 1 allocates TMEM and, in CTA 0, one lane issues the MMAs for the pair,
+// warps 2-9 (two warpgroups, one per 128-column half) drain two TMEM
+// accumulators (double buffered, 2 x 256 columns) so an epilogue overlaps the
+// next tile's main loop.  Every wait is
 // bounded: on time-out a CTA raises an abort flag, lets copies in flight
 // land, frees TMEM and returns, and the workspace status word records
 // STATUS_TIMEOUT.
