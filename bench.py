@@ -201,6 +201,96 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# widened forms of the path (one GPU, one JSON line each; not the contract line)
+# ---------------------------------------------------------------------------
+def run_variant(args) -> int:
+    """Time one widened form of the path at the chosen workload:
+
+    rmsnorm         the final RMSNorm fused in front (flce_rmsnorm_fwd_bwd)
+    autograd        LinearCrossEntropy forward + backward with grad_output 2.5
+                    (the library call plus the flce_scale_grads pass)
+    vocab_parallel  one rank's share of a vocabulary-parallel LM head over
+                    --shards ranks: shard statistics, the lse finish (the
+                    exchange between them is three N-float all-reduces, left
+                    out on one GPU) and the shard backward
+    """
+    import numpy as np
+    import torch
+    from linear_cross_entropy_ce_gb300 import flce, workloads as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flce.library()
+    w = wl.WORKLOADS[args.workload]
+    p = wl.make_inputs(w)
+    N, H, V = w.N, w.H, w.V
+    h = torch.from_numpy(p["hidden"].view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(p["weight"].view(np.int16)).view(torch.bfloat16).to(dev)
+    t = torch.from_numpy(p["targets"]).to(dev)
+    nv = int((p["targets"] != -100).sum())
+    flops = 6.0 * nv * H * V
+    cfg = {"workload": w.name, "N": N, "H": H, "V": V, "n_valid": nv}
+
+    if args.variant == "rmsnorm":
+        gain = (1.0 + 0.1 * torch.randn(H, generator=torch.Generator().manual_seed(5))).to(torch.bfloat16).to(dev)
+        ws = flce.new_workspace(flce.library().flce_rmsnorm_workspace_bytes(N, H, V, 0), dev)
+        out = {}
+
+        def step():
+            flce.rmsnorm_fwd_bwd(h, gain, W, t, workspace=ws, out=out)
+        cfg["workspace_bytes"] = ws.numel()
+    elif args.variant == "autograd":
+        hp = h.clone().requires_grad_(True)
+        Wp = W.clone().requires_grad_(True)
+        g = torch.full((), 2.5, device=dev)
+
+        def step():
+            hp.grad = None
+            Wp.grad = None
+            loss = flce.linear_cross_entropy(hp, Wp, t)
+            loss.backward(g)
+    elif args.variant == "vocab_parallel":
+        P = args.shards
+        Vs = (V + P - 1) // P
+        Wsh = W[:Vs].contiguous()
+        ws_s = flce.new_workspace(flce.library().flce_vocab_shard_workspace_bytes(N, H, Vs, 0), dev)
+        ws_b = flce.new_workspace(flce.library().flce_vocab_shard_workspace_bytes(N, H, Vs, 0), dev)
+
+        def step():
+            st = flce.vocab_shard_stats(h, Wsh, t, 0, V, workspace=ws_s)
+            fin = flce.vocab_finish(st["row_max"], st["row_sumexp"], st["row_target_logit"], t)
+            flce.vocab_shard_bwd(h, Wsh, t, fin["lse"], 0, V, workspace=ws_b)
+        flops = 6.0 * nv * H * Vs
+        cfg.update({"shards": P, "V_shard": Vs, "flops_note": "per-rank share 6*n_valid*H*V/P; the shard "
+                    "backward recomputes the shard's logits (8*N*H*V/P actual)"})
+    else:
+        raise SystemExit(f"unknown variant {args.variant}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_id_for(0))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    pk, src = peaks()
+    line = {"metric": METRIC, "variant": args.variant, "value": N / (ms / 1000.0), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "pct_bf16_peak": {"value": 100.0 * flops / (ms / 1000.0) / 1e12 / float(pk["bf16_tflops"]),
+                              "basis": f"{src} bf16 burst peak"},
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def main():
@@ -216,11 +306,16 @@ def main():
     ap.add_argument("--chunk-rows", type=int, default=None, help="override the default 5%% plan")
     ap.add_argument("--workspace-bytes", type=int, default=None,
                     help="workspace size to plan for (small profiling cases that keep a full-size plan)")
+    ap.add_argument("--variant", default=None, choices=["rmsnorm", "autograd", "vocab_parallel"],
+                    help="time a widened form of the path instead (one GPU; not the contract line)")
+    ap.add_argument("--shards", type=int, default=2, help="vocabulary shards for --variant vocab_parallel")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "flce":
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.variant:
+        return run_variant(args)
 
     import numpy as np
     import torch
