@@ -61,6 +61,23 @@ def test_default_workspace_within_five_percent(lib, name):
     assert p["vocab_tiles"] == -(-V // 256)
 
 
+# Default plans at the benchmark workloads (76 CTA pairs assumed when no GPU is
+# visible): chunk rows and grad_hidden vocabulary splits.  The Llama-3-8B head
+# has no room for the split accumulator inside 5% of its logits; the component
+# shape cannot spread its split units through the few grad_weight units, so
+# the split count balances unit length against the ordered chain of splits.
+PLANS = {"component": (128, 4), "full_model": (2944, 1), "llama3_8b_head": (768, 1), "large_vocab": (384, 16),
+         "large_vocab_tail": (384, 16)}
+
+
+@pytest.mark.parametrize("name", sorted(PLANS))
+def test_default_plans(lib, name):
+    from linear_cross_entropy_ce_gb300 import flce
+    N, H, V = WORKLOADS[name]
+    p = flce.plan(N, H, V, flce.workspace_bytes(N, H, V))
+    assert (p["chunk_rows"], p["dx_splits"]) == PLANS[name]
+
+
 def test_plan_monotone_and_minimum(lib):
     from linear_cross_entropy_ce_gb300 import flce
     N, H, V = 1000, 64, 3000
