@@ -132,15 +132,39 @@ def gpu_id_for(dev_index: int) -> str:
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample_time(p, rows):
-    """Run the fp64 oracle, as it stands, on the first `rows` valid tokens."""
-    import numpy as np
-    from oracle import flce_oracle
-    t = p["targets"]
-    sel = np.nonzero(t != -100)[0][:rows]
-    t0 = time.perf_counter()
-    flce_oracle(p["hidden"][sel], p["weight"], t[sel])
-    return time.perf_counter() - t0, int(sel.size)
+class OracleSampler:
+    """The fp64 oracle, as it stands, timed on samples of one workload.
+
+    One sample = the full forward+backward of the oracle (steps 2-8 of
+    ``oracle.flce_oracle_f64``: logits, log-sum-exp, losses, dz, grad_hidden
+    and grad_weight) on the first `rows` valid tokens with the whole weight.
+    The bf16 -> fp64 decode of the weight (4.2 GB of fp64 at the Llama-3-8B
+    head) is done once, outside every timed sample, so that a sample measures
+    the oracle's arithmetic and not a fixed decoding cost.  The benchmark's
+    cpu_baseline leg and the --impl reference arm use the same sample size,
+    chosen from a 64-row probe to take about `step_s` seconds."""
+
+    def __init__(self, p, step_s=3.0):
+        import numpy as np
+        from oracle import decode_bf16
+        self.p = p
+        self.W64 = decode_bf16(p["weight"])
+        self.valid = np.nonzero(p["targets"] != -100)[0]
+        dt = self.time(64)
+        self.rows = int(max(64, min(4096, self.valid.size, 64 * step_s / max(dt, 1e-3))))
+
+    def time(self, rows=None):
+        from oracle import decode_bf16, flce_oracle_f64
+        sel = self.valid[:rows or self.rows]
+        X64 = decode_bf16(self.p["hidden"][sel])
+        t0 = time.perf_counter()
+        flce_oracle_f64(X64, self.W64, self.p["targets"][sel])
+        return time.perf_counter() - t0
+
+    def sample_name(self):
+        w = self.p["workload"]
+        return (f"fp64 numpy oracle, full fwd+bwd of the first {self.rows} valid tokens of {w.name} "
+                f"(H={w.H}, V={w.V}, full weight, weight decoded once outside the timing) per step")
 
 
 def cpu_cores():
@@ -154,19 +178,12 @@ def cpu_cores():
     return os.cpu_count()
 
 
-def cpu_baseline(p, target_s=12.0):
-    # grow the sample until it is about 10-30 s of CPU work
-    rows = 16
-    dt, n = oracle_sample_time(p, rows)
-    for _ in range(4):
-        if dt >= 10.0 or n < rows:
-            break
-        rows = int(max(rows + 16, min(8192, rows * target_s / max(dt, 1e-3))))
-        dt, n = oracle_sample_time(p, rows)
-    w = p["workload"]
-    return {"value": n / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle, full fwd+bwd of the first {n} valid tokens of {w.name} "
-                      f"(H={w.H}, V={w.V}, full weight), {dt:.2f} s"}
+def cpu_baseline(p, steps=4):
+    # a few steps of the sampler (about 10-15 s of CPU work in all)
+    s = OracleSampler(p)
+    ts = [s.time() for _ in range(steps)]
+    return {"value": steps * s.rows / sum(ts), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{s.sample_name()}; {steps} steps, {sum(ts):.2f} s"}
 
 
 def run_reference(args):
@@ -177,16 +194,12 @@ def run_reference(args):
         return 0
     w = wl.WORKLOADS[args.workload]
     p = wl.make_inputs(w)
-    # size each step to about 3 s of CPU work
-    dt, n = oracle_sample_time(p, 8)
-    rows = int(max(8, min(2048, 8 * 3.0 / max(dt, 1e-3))))
+    s = OracleSampler(p)          # the same sample rule as the cpu_baseline leg
     for _ in range(args.warmup):
-        oracle_sample_time(p, rows)
-    times = []
-    for _ in range(args.steps):
-        dt, n = oracle_sample_time(p, rows)
-        times.append(dt)
+        s.time()
+    times = [s.time() for _ in range(args.steps)]
     ms = 1000.0 * sum(times) / len(times)
+    n = s.rows
     value = n / (ms / 1000.0)
     cores = cpu_cores()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
@@ -194,7 +207,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "sample_rows_per_step": n},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"first {n} valid tokens of {w.name} per step, full weight"},
+                             "sample": s.sample_name()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -331,7 +344,12 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    # device memory before the library is loaded (the context exists already)
+    torch.zeros(1, device=dev)
+    torch.cuda.synchronize()
+    free_before_lib = torch.cuda.mem_get_info(dev)[0]
     flce.library()
+    free_after_lib = torch.cuda.mem_get_info(dev)[0]
 
     base = wl.WORKLOADS[args.workload]
     if args.tokens:
@@ -352,15 +370,37 @@ def main():
            "grad_weight": torch.empty((V, H), dtype=torch.float32, device=dev), "row_loss": None}
     stream = torch.cuda.current_stream()
 
-    def step():
+    # every step writes its loss into its own slot, so that a failed step
+    # (its loss is NaN) is seen after the timed loop
+    loss_slots = torch.full((max(args.steps, args.warmup),), float("nan"), dtype=torch.float32, device=dev)
+
+    def step(i):
+        out["loss"] = loss_slots[i:i + 1]
         flce.fwd_bwd(h, W, t, workspace=ws, out=out, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
+    def check_steps(what, losses):
+        st_ = flce.query_status(ws)
+        if st_ != flce.FLCE_OK:
+            raise RuntimeError(f"{what}: device status {flce.STATUS_NAMES[st_]}")
+        if not bool(torch.isfinite(losses).all()):
+            raise RuntimeError(f"{what}: a step reported a NaN loss (device-side failure)")
+
+    # measured extra device memory: what the library's first calls take
+    # beyond the caller's buffers (module load, static data), and what the
+    # caching allocator hands out during a call (nothing: the caller owns every buffer)
     torch.cuda.synchronize()
-    st = flce.query_status(ws)
-    if st != flce.FLCE_OK:
-        raise RuntimeError(f"device status {flce.STATUS_NAMES[st]}")
+    free_before_call = torch.cuda.mem_get_info(dev)[0]
+    reserved_before_call = torch.cuda.memory_reserved(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    alloc_before_call = torch.cuda.memory_allocated(dev)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    free_after_call = torch.cuda.mem_get_info(dev)[0]
+    lib_bytes = (free_before_lib - free_after_lib) + (free_before_call - free_after_call) \
+        - (torch.cuda.memory_reserved(dev) - reserved_before_call)
+    torch_peak_bytes = torch.cuda.max_memory_allocated(dev) - alloc_before_call
+    check_steps("warm-up", loss_slots[:args.warmup])
 
     clocks = ClockSampler(gpu_id_for(local))
     clocks.start()
@@ -370,14 +410,15 @@ def main():
     flce.profile_begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     prof = flce.profile_end()
     clk = clocks.stop()
+    check_steps("timed steps", loss_slots[:args.steps])
     ms = fdist.max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
 
     # end to end through the public API: pinned host inputs in, loss out, every step
@@ -385,26 +426,28 @@ def main():
     if not args.no_e2e:
         h_host = torch.from_numpy(p["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
         t_host = torch.from_numpy(p["targets"]).pin_memory()
-        loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
+        loss_host = torch.full((args.steps + 2, 2), float("nan"), dtype=torch.float32).pin_memory()
         h_dev, t_dev = torch.empty_like(h), torch.empty_like(t)
+        out["loss"] = loss_slots[0:1]
 
-        def e2e_step():
+        def e2e_step(i):
             h_dev.copy_(h_host, non_blocking=True)
             t_dev.copy_(t_host, non_blocking=True)
             flce.fwd_bwd(h_dev, W, t_dev, workspace=ws, out=out, stream=stream)
-            loss_host[0:1].copy_(out["loss"], non_blocking=True)
-            loss_host[1:2].copy_(out["n_valid"].view(torch.float32), non_blocking=True)
-        for _ in range(2):
-            e2e_step()
+            loss_host[i, 0:1].copy_(out["loss"], non_blocking=True)
+            loss_host[i, 1:2].copy_(out["n_valid"].view(torch.float32), non_blocking=True)
+        for i in range(2):
+            e2e_step(args.steps + i)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        for i in range(args.steps):
+            e2e_step(i)
         a1.record(stream)
         torch.cuda.synchronize()
+        check_steps("e2e steps", loss_host[:, 0])
         e2e_ms = fdist.max_over_ranks(a0.elapsed_time(a1) / args.steps, dev)
         e2e = {"value": world * N / (e2e_ms / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": N * H * 2 + N * 4, "d2h_bytes_per_step": 8,
@@ -449,6 +492,14 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "N": N, "H": H, "V": V, "n_valid": nv, "chunk_rows": plan["chunk_rows"],
                    "workspace_bytes": ws_bytes, "extra_mem_frac_of_NV2": ws_bytes / (N * V * 2),
+                   "extra_mem_measured": {
+                       "workspace_bytes": ws_bytes, "library_device_bytes": lib_bytes,
+                       "torch_alloc_peak_bytes": torch_peak_bytes,
+                       "frac_of_NV2": (ws_bytes + max(0, lib_bytes) + torch_peak_bytes) / (N * V * 2),
+                       "how": "library_device_bytes: cudaMemGetInfo free-memory drop across loading libflce.so and "
+                              "its warm-up calls, minus what the caching allocator reserved meanwhile (module code "
+                              "and static device data); torch_alloc_peak_bytes: max_memory_allocated during the "
+                              "calls minus allocated before them"},
                    "l2": "inputs larger than L2 (weight alone exceeds 129 MB), no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_bf16_peak": {"value": 100.0 * step_tflops / peak_b, "tflops_alg": step_tflops,

@@ -40,7 +40,9 @@
  * returned at once and nothing is enqueued.  Errors that only the device can
  * see (a target outside [0, V) that is not ignore_index, a stalled pipeline
  * stage) are recorded in a status word inside the workspace: read it with
- * flce_query_status().  Device code never traps.
+ * flce_query_status().  The loss of a call whose device status is not FLCE_OK is
+ * written as NaN, so a caller that never reads the status still sees that the
+ * outputs of that call are not valid.  Device code never traps.
  *
  * Concurrency.  Calls are reentrant; concurrent calls need separate
  * workspaces.
@@ -69,6 +71,18 @@ typedef enum flce_status {
 /* Reduction flags (bit 0). */
 #define FLCE_REDUCE_MEAN 0x0u  /* mean over non-ignored tokens (default)       */
 #define FLCE_REDUCE_SUM  0x1u  /* unscaled sum; grads without the 1/n_valid   */
+/*
+ * Output precision of grad_weight (bit 1), flce_fwd_bwd and
+ * flce_rmsnorm_fwd_bwd only.  With FLCE_GW_BF16, grad_weight is a bf16
+ * [V,H] array: the gradient still accumulates in fp32 over the token chunks
+ * ("Alisa's book of LLMs", "Precision": bf16 compute, fp32 accumulation of
+ * gradients) in a V*H*4-byte region of the workspace, and the finished sum is
+ * rounded once (nearest even) into grad_weight.  The workspace functions
+ * include that region when the flag is passed, so this workspace is larger
+ * than 5% of the bf16 logits at every large vocabulary (V*H*4 alone is
+ * 2.1 GB at H=4096, V=128256).
+ */
+#define FLCE_GW_BF16     0x2u
 
 /* Description of how a call is carried out for a given workspace size. */
 typedef struct flce_plan_info {
@@ -113,7 +127,7 @@ flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags,
  *   n_valid      [1] int32 (device)           written: tokens with t != ignore_index
  *   row_loss     [N] fp32 (device) or NULL    written: loss_n (unscaled), 0 when ignored
  *   grad_hidden  [N,H] bf16 (device)          written
- *   grad_weight  [V,H] fp32 (device)          written
+ *   grad_weight  [V,H] fp32 (device)          written (bf16 with FLCE_GW_BF16)
  *   workspace    device scratch of workspace_bytes (>= flce_workspace_bytes_for_chunk
  *                with chunk 128); its contents need no initialisation and
  *                hold the device status word afterwards.
@@ -229,6 +243,28 @@ flce_status flce_scale_grads(void* grad_hidden, float* grad_weight, int64_t N,
  * FLCE_ECUDA if the stream reports an error).
  */
 flce_status flce_query_status(const void* workspace, void* stream);
+
+/*
+ * Where the first pipeline wait of the last call on `workspace` ran out of
+ * time (after FLCE_ETIMEOUT).  Synchronises `stream`.  info[0] = wait site
+ * (0 = none; 10 = an epilogue waiting for its accumulator, 6 = the MMA
+ * issuer waiting for a free accumulator, 7 = the MMA issuer waiting for
+ * operands, 3 = the TMA producer waiting for a free stage; the others are
+ * the scheduler hand-offs), info[1] = CTA rank in its pair, info[2] = block
+ * index, info[3] = number of waits that ran out.
+ */
+flce_status flce_query_stall(const void* workspace, int32_t* info /* [4] */, void* stream);
+
+/*
+ * Test hook for the failure path of the GEMM pipeline: arms the next tcgen05
+ * GEMM launch of this process (a one-shot, process-wide switch) so that its
+ * MMA issuer withholds the accumulator-ready signal of the first tile of every
+ * CTA pair.  The epilogue's bounded wait for that signal then runs out after
+ * timeout_ns (<= 10 s); the kernel raises its abort flag, lets the copies in
+ * flight land, waits for its MMAs, frees TMEM and returns.  The call's status
+ * becomes FLCE_ETIMEOUT and its loss NaN; the CUDA context stays usable.
+ */
+flce_status flce_debug_arm_stall(uint64_t timeout_ns);
 
 /*
  * Diagnostic: enqueue one kernel that waits on a pipeline barrier nothing

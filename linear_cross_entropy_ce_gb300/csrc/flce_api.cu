@@ -13,6 +13,7 @@
 // The only buffer that scales with V is the C x V bf16 chunk of logits, so
 // the default plan keeps the workspace below 5% of the N x V bf16 logits.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -90,9 +91,9 @@ struct Plan {
   long long N = 0, H = 0, V = 0, C = 0, ldz = 0, n_chunks = 0;
   int nvt = 0, nparts = 0, splits = 1, kb_per_split = 0;
   long long n_counters = 0, flags_per_chunk = 0;
-  bool fwd_only = false, norm = false;
+  bool fwd_only = false, norm = false, gw32 = false;
   size_t o_idx = 0, o_rl = 0, o_cnt = 0, o_xc = 0, o_tc = 0, o_zt = 0, o_part = 0, o_z = 0, o_dx = 0, o_rinv = 0,
-         o_dg = 0, total = 0;
+         o_dg = 0, o_gw = 0, total = 0;
 };
 
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -103,10 +104,12 @@ constexpr int MAX_SPLITS = 16;   // splits are summed one after another: keep th
 constexpr int DX_UNIT_KB = 128;  // preferred K blocks of one dX unit
 
 // Workspace layout for chunks of C rows.  Only the bf16 C x V logits buffer
-// (absent for the forward-only call) grows with V.
-Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_only, bool norm = false) {
+// (absent for the forward-only call) grows with V; with a bf16 grad_weight
+// (gw32) the fp32 V x H accumulator of grad_weight lives here as well.
+Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_only, bool norm = false,
+            bool gw32 = false) {
   Plan p;
-  p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only; p.norm = norm;
+  p.N = N; p.H = H; p.V = V; p.C = C; p.fwd_only = fwd_only; p.norm = norm; p.gw32 = gw32 && !fwd_only;
   p.ldz = cdiv(V, 64) * 64;
   p.nvt = static_cast<int>(cdiv(V, BN));
   p.nparts = static_cast<int>(cdiv(V, PART_COLS));
@@ -133,6 +136,7 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
     p.o_rinv = off; off += al256(size_t(C) * 4);
     p.o_dg = off;   off += al256(size_t(p.n_chunks) * H * 4);
   }
+  if (p.gw32) { p.o_gw = off; off += al256(size_t(V) * H * 4); }
   p.total = off;
   return p;
 }
@@ -169,23 +173,23 @@ int preferred_splits(long long C, long long H, long long V, int pairs) {
 long long max_chunk(long long N) { return cdiv(N, BM) * BM; }
 
 Plan plan_for_chunk(long long N, long long H, long long V, long long C, bool fwd_only, int pairs, size_t bytes,
-                    bool norm = false) {
-  Plan p = layout(N, H, V, C, preferred_splits(C, H, V, pairs), fwd_only, norm);
-  if (p.total > bytes) p = layout(N, H, V, C, 1, fwd_only, norm);
+                    bool norm = false, bool gw32 = false) {
+  Plan p = layout(N, H, V, C, preferred_splits(C, H, V, pairs), fwd_only, norm, gw32);
+  if (p.total > bytes) p = layout(N, H, V, C, 1, fwd_only, norm, gw32);
   return p;
 }
 
 // Largest chunk (multiple of 128 rows) whose plan fits in `bytes`.
 bool plan_for_bytes(long long N, long long H, long long V, bool fwd_only, size_t bytes, int pairs, Plan* out,
-                    bool norm = false) {
+                    bool norm = false, bool gw32 = false) {
   long long lo = BM, hi = max_chunk(N);
-  if (layout(N, H, V, lo, 1, fwd_only, norm).total > bytes) return false;
+  if (layout(N, H, V, lo, 1, fwd_only, norm, gw32).total > bytes) return false;
   while (lo < hi) {   // the size shrinks as C grows only through the d(gain) partials: bisect on the total
     const long long mid = ((lo / BM + hi / BM + 1) / 2) * BM;
-    if (layout(N, H, V, mid, 1, fwd_only, norm).total <= bytes) lo = mid;
+    if (layout(N, H, V, mid, 1, fwd_only, norm, gw32).total <= bytes) lo = mid;
     else hi = mid - BM;
   }
-  *out = plan_for_chunk(N, H, V, lo, fwd_only, pairs, bytes, norm);
+  *out = plan_for_chunk(N, H, V, lo, fwd_only, pairs, bytes, norm, gw32);
   return true;
 }
 
@@ -200,14 +204,20 @@ bool sizes_ok(long long N, long long H, long long V) {
   return N >= 1 && H >= 8 && V >= 1 && N < (1ll << 31) && V < (1ll << 31) && H <= (1ll << 20) && H % 8 == 0;
 }
 
-size_t default_bytes(long long N, long long H, long long V, bool fwd_only, bool norm = false) {
+// The default plan: chunk buffers within 5% of the bf16 logits (never below
+// one 128-row chunk), plus the fp32 grad_weight accumulator when the caller
+// asked for a bf16 grad_weight.
+size_t default_bytes(long long N, long long H, long long V, bool fwd_only, bool norm = false, bool gw32 = false) {
   if (!sizes_ok(N, H, V)) return 0;
-  const size_t budget = size_t(N) * size_t(V) * 2 / 20;   // 5% of the bf16 logits
+  gw32 = gw32 && !fwd_only;
+  const size_t budget = size_t(N) * size_t(V) * 2 / 20 + (gw32 ? al256(size_t(V) * H * 4) : 0);
   const int pairs = device_pairs();
   Plan p;
-  if (plan_for_bytes(N, H, V, fwd_only, budget, pairs, &p, norm)) return p.total;
-  return plan_for_chunk(N, H, V, BM, fwd_only, pairs, ~size_t(0), norm).total;   // never below one 128-row chunk
+  if (plan_for_bytes(N, H, V, fwd_only, budget, pairs, &p, norm, gw32)) return p.total;
+  return plan_for_chunk(N, H, V, BM, fwd_only, pairs, ~size_t(0), norm, gw32).total;
 }
+
+constexpr uint32_t KNOWN_FLAGS = FLCE_REDUCE_SUM | FLCE_GW_BF16;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -260,8 +270,17 @@ cudaEvent_t prof_event() {
   return e;
 }
 
+// Test hook (flce_debug_arm_stall): a non-zero value arms the next GEMM
+// launch of the process to withhold one pipeline signal, with this wait limit.
+std::atomic<unsigned long long> g_stall_armed{0};
+
 // Launch a GEMM, bracketed by events when profiling is on.
-cudaError_t gemm_launch(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t st) {
+cudaError_t gemm_launch(const GemmArgs& g0, const GemmMaps& m, int grid, cudaStream_t st) {
+  GemmArgs g = g0;
+  if (const unsigned long long t = g_stall_armed.exchange(0)) {
+    g.debug_stall = 1;
+    g.timeout_ns = t;
+  }
   Profiler& p = prof();
   std::unique_lock<std::mutex> lk(p.mu);
   if (!p.on) {
@@ -303,7 +322,7 @@ struct Job {
   float* row_loss = nullptr;
   void* grad_hidden = nullptr;       // bf16 [N, H], or fp32 when grad_hidden_f32
   bool grad_hidden_f32 = false;
-  float* grad_weight = nullptr;
+  float* grad_weight = nullptr;      // fp32 [V, H], or bf16 when FLCE_GW_BF16 is set
   const void* gain = nullptr;        // final RMSNorm
   float eps = 0.f;
   float* grad_gain = nullptr;
@@ -326,7 +345,9 @@ flce_status run(const Job& j) {
   if (!fwd_only && (!j.grad_hidden || !j.grad_weight)) return FLCE_EINVAL;
   if (j.kind == JOB_SHARD_STATS && (!j.row_max || !j.row_sumexp || !j.row_zt)) return FLCE_EINVAL;
   if (j.kind == JOB_SHARD_BWD && !j.lse) return FLCE_EINVAL;
-  if (j.flags & ~FLCE_REDUCE_SUM) return FLCE_EINVAL;
+  if (j.flags & ~KNOWN_FLAGS) return FLCE_EINVAL;
+  const bool gw_bf16 = (j.flags & FLCE_GW_BF16) != 0;
+  if (gw_bf16 && j.kind != JOB_FWD_BWD) return FLCE_EINVAL;   // forward-only and shard calls have no such output
   if (N < 1 || H < 1 || V < 1 || j.v0 < 0 || j.V_total < j.v0 + V) return FLCE_EINVAL;
   if (!sizes_ok(N, H, V) || j.V_total >= (1ll << 31)) return FLCE_EUNSUPPORTED;
   if (!aligned16(j.hidden) || !aligned16(j.weight) || !aligned16(j.ws) || !aligned4(j.targets) ||
@@ -339,7 +360,7 @@ flce_status run(const Job& j) {
   if (device_state(&dev) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
   if (dev.major < 10) return FLCE_EUNSUPPORTED;
   Plan p;
-  if (!plan_for_bytes(N, H, V, fwd_only, j.ws_bytes, dev.pairs, &p, norm)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, fwd_only, j.ws_bytes, dev.pairs, &p, norm, gw_bf16)) return FLCE_EWORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(j.stream);
   void* ws = j.ws;
@@ -355,6 +376,9 @@ flce_status run(const Job& j) {
   float* dxacc = (!fwd_only && p.splits > 1) ? at<float>(ws, p.o_dx) : nullptr;
   float* rinv = norm ? at<float>(ws, p.o_rinv) : nullptr;
   float* dgp = norm ? at<float>(ws, p.o_dg) : nullptr;
+  // the fp32 accumulator of grad_weight: the output itself, or a workspace
+  // region that is rounded to the bf16 output at the end
+  float* gwacc = p.gw32 ? at<float>(ws, p.o_gw) : j.grad_weight;
 
   GemmMaps fm, bm;   // forward (logits) and backward (dX + dW) launches
   std::memset(&fm, 0, sizeof(fm));
@@ -364,9 +388,9 @@ flce_status run(const Job& j) {
   if (!fwd_only)
     ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, j.weight, H, V, hb, 64, BK) &&
          make_map(&bm.a1, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&bm.b1, xc, H, p.C, hb, 64, BK) &&
-         make_map(&bm.out, j.grad_weight, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
+         make_map(&bm.out, gwacc, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         make_map(&bm.pf, j.grad_weight, H, V, static_cast<unsigned long long>(H) * 4, BN, BM,
+         make_map(&bm.pf, gwacc, H, V, static_cast<unsigned long long>(H) * 4, BN, BM,
                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE) &&
          (!dxacc || make_map(&bm.dx, dxacc, H, p.C, static_cast<unsigned long long>(H) * 4, 16, BM,
                              CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B));
@@ -392,7 +416,7 @@ flce_status run(const Job& j) {
   g.idx = idx;
   g.grad_hidden = j.grad_hidden_f32 ? nullptr : static_cast<uint16_t*>(j.grad_hidden);
   g.grad_hidden_f32 = j.grad_hidden_f32 ? static_cast<float*>(j.grad_hidden) : nullptr;
-  g.grad_weight = j.grad_weight;
+  g.grad_weight = gwacc;
   g.splits = p.splits;
   g.kb_per_split = p.kb_per_split;
   g.interleave = 1;
@@ -413,7 +437,7 @@ flce_status run(const Job& j) {
   const bool stats = j.kind == JOB_SHARD_STATS;
   const int v0 = static_cast<int>(j.v0);
   count_launches(1 + (fwd_only ? 0 : 1) + (j.kind == JOB_SHARD_BWD ? 0 : 1) + p.n_chunks * (norm ? 4 : 2) +
-                 (norm ? 1 : 0));
+                 (norm ? 1 : 0) + (p.gw32 ? 1 : 0));
   if (!chk(launch_prep(j.targets, N, static_cast<int>(j.V_total), j.ii, hdr, idx, j.n_valid, counters,
                        p.n_counters, st)))
     return FLCE_ECUDA;
@@ -461,6 +485,8 @@ flce_status run(const Job& j) {
     if (!chk(launch_finalize(hdr, idx, rl, N, reduce_sum, j.loss, j.n_valid, j.row_loss, st))) return FLCE_ECUDA;
   }
   if (norm && !chk(launch_dgain_reduce(dgp, p.n_chunks, g.H, j.grad_gain, st))) return FLCE_ECUDA;
+  if (p.gw32 && !chk(launch_f32_to_bf16(gwacc, V * H, reinterpret_cast<uint16_t*>(j.grad_weight), st)))
+    return FLCE_ECUDA;
   return FLCE_OK;
 }
 
@@ -497,8 +523,8 @@ flce_status fwd_bwd_on_workspace(const void* hidden, const void* weight, const i
 extern "C" {
 
 size_t flce_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags) {
-  if (flags & ~FLCE_REDUCE_SUM) return 0;
-  return default_bytes(N, H, V, false);
+  if (flags & ~KNOWN_FLAGS) return 0;
+  return default_bytes(N, H, V, false, false, (flags & FLCE_GW_BF16) != 0);
 }
 
 size_t flce_loss_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags) {
@@ -507,19 +533,21 @@ size_t flce_loss_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags
 }
 
 size_t flce_workspace_bytes_for_chunk(int64_t N, int64_t H, int64_t V, uint32_t flags, int64_t chunk_rows) {
-  if ((flags & ~FLCE_REDUCE_SUM) || !sizes_ok(N, H, V) || chunk_rows < 1) return 0;
+  if ((flags & ~KNOWN_FLAGS) || !sizes_ok(N, H, V) || chunk_rows < 1) return 0;
   long long C = cdiv(chunk_rows, BM) * BM;
   if (C > max_chunk(N)) C = max_chunk(N);
-  return plan_for_chunk(N, H, V, C, false, device_pairs(), ~size_t(0)).total;
+  return plan_for_chunk(N, H, V, C, false, device_pairs(), ~size_t(0), false, (flags & FLCE_GW_BF16) != 0).total;
 }
 
 flce_status flce_plan(int64_t N, int64_t H, int64_t V, uint32_t flags, int forward_only, size_t workspace_bytes,
                       flce_plan_info* out) {
-  if (!out || (flags & ~FLCE_REDUCE_SUM)) return FLCE_EINVAL;
+  if (!out || (flags & ~KNOWN_FLAGS)) return FLCE_EINVAL;
   if (N < 1 || H < 1 || V < 1) return FLCE_EINVAL;
   if (!sizes_ok(N, H, V)) return FLCE_EUNSUPPORTED;
   Plan p;
-  if (!plan_for_bytes(N, H, V, forward_only != 0, workspace_bytes, device_pairs(), &p)) return FLCE_EWORKSPACE;
+  if (!plan_for_bytes(N, H, V, forward_only != 0, workspace_bytes, device_pairs(), &p, false,
+                      (flags & FLCE_GW_BF16) != 0))
+    return FLCE_EWORKSPACE;
   out->chunk_rows = p.C;
   out->max_chunks = p.n_chunks;
   out->logits_row_stride = p.ldz;
@@ -560,9 +588,32 @@ flce_status flce_query_status(const void* workspace, void* stream) {
   return FLCE_OK;
 }
 
+flce_status flce_query_stall(const void* workspace, int32_t* info, void* stream) {
+  if (!workspace || !aligned16(workspace) || !info) return FLCE_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) { cudaGetLastError(); return FLCE_ECUDA; }
+  int w[2] = {0, 0};   // HDR_STALL, HDR_STALL_COUNT
+  if (cudaMemcpy(w, static_cast<const int*>(workspace) + HDR_STALL, sizeof(w), cudaMemcpyDeviceToHost) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return FLCE_ECUDA;
+  }
+  info[0] = w[0] & 0xff;
+  info[1] = (w[0] >> 8) & 0xf;
+  info[2] = w[0] >> 12;
+  info[3] = w[1];
+  return FLCE_OK;
+}
+
+flce_status flce_debug_arm_stall(uint64_t timeout_ns) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FLCE_EINVAL;
+  g_stall_armed.store(timeout_ns);
+  return FLCE_OK;
+}
+
 size_t flce_rmsnorm_workspace_bytes(int64_t N, int64_t H, int64_t V, uint32_t flags) {
-  if (flags & ~FLCE_REDUCE_SUM) return 0;
-  return default_bytes(N, H, V, false, true);
+  if (flags & ~KNOWN_FLAGS) return 0;
+  return default_bytes(N, H, V, false, true, (flags & FLCE_GW_BF16) != 0);
 }
 
 flce_status flce_rmsnorm_fwd_bwd(const void* hidden, const void* gain, float eps, const void* weight,

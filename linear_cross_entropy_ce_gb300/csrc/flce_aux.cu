@@ -249,7 +249,12 @@ __global__ void __launch_bounds__(FIN_THREADS)
   for (long long i = threadIdx.x; i < nv; i += FIN_THREADS) s += rl[i];
   s = block_reduce(s, AddOp(), 0.0, red);
   if (threadIdx.x == 0) {
-    *loss = nv == 0 ? 0.f : static_cast<float>(reduce_sum ? s : s / static_cast<double>(nv));
+    // A call whose device status is not OK (a bad target, a pipeline
+    // time-out) reports a NaN loss, so that callers who never read the status
+    // word still see that the outputs are not to be trusted.
+    const bool failed = hdr[HDR_STATUS] != 0;
+    *loss = failed ? __int_as_float(0x7fc00000)
+                   : (nv == 0 ? 0.f : static_cast<float>(reduce_sum ? s : s / static_cast<double>(nv)));
     if (n_valid_out) *n_valid_out = static_cast<int>(nv);
   }
   if (row_loss)
@@ -509,6 +514,17 @@ __global__ void timeout_selftest_kernel(int* hdr, unsigned long long timeout_ns)
   if (!done) atomicOr(&hdr[HDR_STATUS], STATUS_TIMEOUT);
 }
 
+// The fp32 grad_weight accumulator rounded once to the bf16 output
+// (FLCE_GW_BF16): gradients accumulate in fp32 and only the finished sum is
+// stored at the parameter's precision ("Alisa's book of LLMs", "Precision").
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ src, long long n4, uint2* __restrict__ dst) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 v = __ldcs(src + i);
+    dst[i] = make_uint2(ptx::pack_bf16x2(v.x, v.y), ptx::pack_bf16x2(v.z, v.w));
+  }
+}
+
 inline int grid_for(long long work, int threads, int cap) {
   long long g = (work + threads - 1) / threads;
   if (g < 1) g = 1;
@@ -603,6 +619,13 @@ cudaError_t launch_scale_grads(uint16_t* grad_hidden, long long n_hidden, float*
                                const float* scale, cudaStream_t s) {
   const long long n8 = n_hidden / 8, n4 = n_weight / 4;
   scale_grads_kernel<<<grid_for(n8 > n4 ? n8 : n4, 256, 152 * 8), 256, 0, s>>>(grad_hidden, n8, grad_weight, n4, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, long long n, uint16_t* dst, cudaStream_t s) {
+  const long long n4 = n / 4;
+  f32_to_bf16_kernel<<<grid_for(n4, 256, 152 * 8), 256, 0, s>>>(reinterpret_cast<const float4*>(src), n4,
+                                                                reinterpret_cast<uint2*>(dst));
   return cudaGetLastError();
 }
 

@@ -572,6 +572,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1 && lane == 0 && lead) {
     // ---------------- MMA issuer for the pair ----------------
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, sslot = 0, sphase = 0;
+    bool withhold = a.debug_stall != 0;   // test hook, see GemmArgs::debug_stall
     for (;;) {
       if (!wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_MMA)) break;
       const int u = ctl->sunit[sslot];
@@ -603,7 +604,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         if (++stage == nstages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      ptx::umma_commit_pair(&ctl->tfull[acc], PAIR_MASK);       // accumulator ready in both CTAs
+      if (!withhold) ptx::umma_commit_pair(&ctl->tfull[acc], PAIR_MASK);   // accumulator ready in both CTAs
+      withhold = false;
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }

@@ -59,6 +59,8 @@ struct GemmArgs {
                         // (else one TMA prefetch when the tile's main loop starts)
   int* flags;           // BWD, splits > 1: per (tile, CTA, warpgroup) count of finished splits (zero before)
   unsigned long long timeout_ns;
+  int debug_stall;      // test hook: the MMA issuer withholds the accumulator-ready signal of each
+                        // pair's first unit, so that the epilogue's bounded wait runs out
   // epilogue operands
   uint16_t* z;          // [C][ldz] bf16
   float2* part;         // [C][nparts] (part max, part sum of exp)
@@ -125,5 +127,7 @@ cudaError_t launch_scale_grads(uint16_t* grad_hidden, long long n_hidden, float*
                                long long n_weight, const float* scale, cudaStream_t s);
 cudaError_t launch_timeout_selftest(int* hdr, unsigned long long timeout_ns,
                                     cudaStream_t s);
+// fp32 -> bf16 (round to nearest even), n a multiple of 4, both 16-byte aligned
+cudaError_t launch_f32_to_bf16(const float* src, long long n, uint16_t* dst, cudaStream_t s);
 
 }  // namespace flce

@@ -21,6 +21,7 @@ FLCE_OK, FLCE_EINVAL, FLCE_EUNSUPPORTED, FLCE_EWORKSPACE, FLCE_EBADTARGET, FLCE_
 STATUS_NAMES = {0: "FLCE_OK", 1: "FLCE_EINVAL", 2: "FLCE_EUNSUPPORTED", 3: "FLCE_EWORKSPACE",
                 4: "FLCE_EBADTARGET", 5: "FLCE_ETIMEOUT", 6: "FLCE_ECUDA"}
 REDUCE = {"mean": 0, "sum": 1}
+FLCE_GW_BF16 = 0x2
 
 _lib = None
 
@@ -64,6 +65,10 @@ def library() -> ctypes.CDLL:
     lib.flce_query_status.restype = ctypes.c_int
     lib.flce_selftest_timeout.argtypes = [vp, ctypes.c_uint64, vp]
     lib.flce_selftest_timeout.restype = ctypes.c_int
+    lib.flce_query_stall.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+    lib.flce_query_stall.restype = ctypes.c_int
+    lib.flce_debug_arm_stall.argtypes = [ctypes.c_uint64]
+    lib.flce_debug_arm_stall.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_rmsnorm_workspace_bytes.argtypes = [i64, i64, i64, u32]
@@ -130,10 +135,18 @@ def _check_inputs(hidden, weight, targets):
     return N, H, V
 
 
+def _flags(reduction: str, grad_weight_dtype=torch.float32) -> int:
+    if grad_weight_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("grad_weight_dtype must be torch.float32 or torch.bfloat16")
+    return REDUCE[reduction] | (FLCE_GW_BF16 if grad_weight_dtype == torch.bfloat16 else 0)
+
+
 def workspace_bytes(N: int, H: int, V: int, reduction: str = "mean", chunk_rows: Optional[int] = None,
-                    forward_only: bool = False) -> int:
+                    forward_only: bool = False, grad_weight_dtype=torch.float32) -> int:
+    """Workspace of the default plan (or of a given chunk size).  With a bf16
+    grad_weight it includes the fp32 V x H accumulator of grad_weight."""
     lib = library()
-    f = REDUCE[reduction]
+    f = _flags(reduction, torch.float32 if forward_only else grad_weight_dtype)
     if forward_only:
         n = lib.flce_loss_workspace_bytes(N, H, V, f)
     elif chunk_rows is not None:
@@ -146,9 +159,10 @@ def workspace_bytes(N: int, H: int, V: int, reduction: str = "mean", chunk_rows:
 
 
 def plan(N: int, H: int, V: int, workspace_bytes: int, forward_only: bool = False,
-         reduction: str = "mean") -> dict:
+         reduction: str = "mean", grad_weight_dtype=torch.float32) -> dict:
     info = PlanInfo()
-    s = library().flce_plan(N, H, V, REDUCE[reduction], int(forward_only), workspace_bytes, ctypes.byref(info))
+    s = library().flce_plan(N, H, V, _flags(reduction, grad_weight_dtype), int(forward_only), workspace_bytes,
+                            ctypes.byref(info))
     if s != FLCE_OK:
         raise FlceError(s, "flce_plan")
     return {k: getattr(info, k) for k, _ in PlanInfo._fields_}
@@ -161,21 +175,26 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 def fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
             reduction: str = "mean", *, workspace: Optional[torch.Tensor] = None,
             chunk_rows: Optional[int] = None, row_loss: bool = False, out: Optional[dict] = None,
-            stream=None) -> dict:
-    """Loss, n_valid, grad_hidden (bf16 [N,H]) and grad_weight (fp32 [V,H]) in one call."""
+            stream=None, grad_weight_dtype=torch.float32) -> dict:
+    """Loss, n_valid, grad_hidden (bf16 [N,H]) and grad_weight ([V,H], fp32 by
+    default, or bf16 rounded once from the fp32 accumulation) in one call."""
     N, H, V = _check_inputs(hidden, weight, targets)
     dev = hidden.device
+    flags = _flags(reduction, grad_weight_dtype)
     if workspace is None:
-        workspace = new_workspace(workspace_bytes(N, H, V, reduction, chunk_rows), dev)
+        workspace = new_workspace(workspace_bytes(N, H, V, reduction, chunk_rows,
+                                                  grad_weight_dtype=grad_weight_dtype), dev)
     o = out if out is not None else {}
     if "loss" not in o:
         o["loss"] = torch.empty(1, dtype=torch.float32, device=dev)
         o["n_valid"] = torch.empty(1, dtype=torch.int32, device=dev)
         o["grad_hidden"] = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-        o["grad_weight"] = torch.empty((V, H), dtype=torch.float32, device=dev)
+        o["grad_weight"] = torch.empty((V, H), dtype=grad_weight_dtype, device=dev)
         o["row_loss"] = torch.empty(N, dtype=torch.float32, device=dev) if row_loss else None
+    if o["grad_weight"].dtype != grad_weight_dtype:
+        raise TypeError("out['grad_weight'] does not have grad_weight_dtype")
     s = library().flce_fwd_bwd(_ptr(hidden), _ptr(weight), _ptr(targets), N, H, V, int(ignore_index),
-                               REDUCE[reduction], _ptr(o["loss"]), _ptr(o["n_valid"]), _ptr(o.get("row_loss")),
+                               flags, _ptr(o["loss"]), _ptr(o["n_valid"]), _ptr(o.get("row_loss")),
                                _ptr(o["grad_hidden"]), _ptr(o["grad_weight"]), _ptr(workspace),
                                workspace.numel(), _stream(stream))
     if s != FLCE_OK:
@@ -363,6 +382,22 @@ def query_status(workspace: torch.Tensor, stream=None) -> int:
 
 def selftest_timeout(workspace: torch.Tensor, timeout_ns: int, stream=None) -> int:
     return int(library().flce_selftest_timeout(_ptr(workspace), int(timeout_ns), _stream(stream)))
+
+
+def query_stall(workspace: torch.Tensor, stream=None) -> dict:
+    """Where the first pipeline wait of the last call ran out of time (site 0: none)."""
+    info = (ctypes.c_int32 * 4)()
+    s = library().flce_query_stall(_ptr(workspace), info, _stream(stream))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_query_stall")
+    return {"site": info[0], "cta_rank": info[1], "block": info[2], "count": info[3]}
+
+
+def debug_arm_stall(timeout_ns: int) -> None:
+    """Test hook: the next GEMM launch withholds one pipeline signal (see flce.h)."""
+    s = library().flce_debug_arm_stall(int(timeout_ns))
+    if s != FLCE_OK:
+        raise FlceError(s, "flce_debug_arm_stall")
 
 
 def profile_begin() -> None:

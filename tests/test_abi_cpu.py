@@ -119,3 +119,33 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.flce_workspace_bytes(16, 63, 32, 0) == 0
     assert lib.flce_query_status(None, None) == flce.FLCE_EINVAL
     assert lib.flce_selftest_timeout(None, 1000, None) == flce.FLCE_EINVAL
+
+
+def test_bf16_grad_weight_flag_sizes_and_rules(lib):
+    # FLCE_GW_BF16 adds the fp32 V x H accumulator of grad_weight to the default plan
+    from linear_cross_entropy_ce_gb300 import flce
+    import torch
+    for N, H, V in [(1000, 64, 3000), WORKLOADS["llama3_8b_head"]]:
+        base = flce.workspace_bytes(N, H, V)
+        with_acc = flce.workspace_bytes(N, H, V, grad_weight_dtype=torch.bfloat16)
+        assert with_acc - base >= V * H * 4
+        assert flce.plan(N, H, V, with_acc, grad_weight_dtype=torch.bfloat16)["chunk_rows"] == \
+            flce.plan(N, H, V, base)["chunk_rows"]
+        # the fp32 plan's bytes are too few once the accumulator is needed
+        with pytest.raises(flce.FlceError):
+            flce.plan(N, H, V, base, grad_weight_dtype=torch.bfloat16)
+    vp = ctypes.c_void_p
+    g = vp(1 << 20)
+    # forward-only and vocabulary-shard calls have no grad_weight to round
+    assert lib.flce_loss(g, g, g, 16, 64, 32, -100, flce.FLCE_GW_BF16, g, g, None, g, 1 << 20, None) == \
+        flce.FLCE_EINVAL
+    assert lib.flce_loss_workspace_bytes(16, 64, 32, flce.FLCE_GW_BF16) == 0
+
+
+def test_debug_and_stall_entry_points_reject_bad_arguments(lib):
+    from linear_cross_entropy_ce_gb300 import flce
+    assert lib.flce_debug_arm_stall(0) == flce.FLCE_EINVAL
+    assert lib.flce_debug_arm_stall(20_000_000_000) == flce.FLCE_EINVAL
+    info = (ctypes.c_int32 * 4)()
+    assert lib.flce_query_stall(None, info, None) == flce.FLCE_EINVAL
+    assert lib.flce_query_stall(ctypes.c_void_p(1 << 20), None, None) == flce.FLCE_EINVAL

@@ -10,6 +10,10 @@ N, H and V.  The full-size workloads run in the launch configuration the
 benchmark uses and are checked on sampled rows the oracle computes one by
 one, plus properties that hold at any size.
 """
+import json
+import math
+import os
+
 import numpy as np
 import pytest
 
@@ -39,7 +43,15 @@ def _flce():
     return flce
 
 
-def check_full(p, dev, chunk_rows=None, reduction="mean"):
+def report(case, **errors):
+    """Append the measured errors of a parity case to $FLCE_PARITY_REPORT (JSON lines), if set."""
+    path = os.environ.get("FLCE_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": case, **{k: float(v) for k, v in errors.items()}}) + "\n")
+
+
+def check_full(p, dev, chunk_rows=None, reduction="mean", case=None):
     flce = _flce()
     h, w, t = to_device(p, dev)
     out = flce.fwd_bwd(h, w, t, reduction=reduction, chunk_rows=chunk_rows, row_loss=True)
@@ -55,8 +67,12 @@ def check_full(p, dev, chunk_rows=None, reduction="mean"):
     gh = gh_np(out["grad_hidden"])
     gw = out["grad_weight"].cpu().double().numpy()
     assert np.all(np.isfinite(gh)) and np.all(np.isfinite(gw))
-    assert frob_rel(gh, ref["grad_hidden"]) <= GRAD_FROB_RTOL
-    assert frob_rel(gw, ref["grad_weight"]) <= GRAD_FROB_RTOL
+    e_gh, e_gw = frob_rel(gh, ref["grad_hidden"]), frob_rel(gw, ref["grad_weight"])
+    assert e_gh <= GRAD_FROB_RTOL
+    assert e_gw <= GRAD_FROB_RTOL
+    if case:
+        report(case, loss=loss_rel(loss, ref["loss"]) if ref["loss"] else abs(loss), grad_hidden=e_gh,
+               grad_weight=e_gw)
     ign = p["targets"] == -100
     if ign.any():
         import torch
@@ -73,7 +89,7 @@ def check_full(p, dev, chunk_rows=None, reduction="mean"):
 # --------------------------------------------------------------------------
 
 def test_tiny_workload(dev):
-    check_full(wl.make_inputs(wl.WORKLOADS["tiny"]), dev)
+    check_full(wl.make_inputs(wl.WORKLOADS["tiny"]), dev, case="tiny")
 
 
 @pytest.mark.parametrize("N,H,V,ign,chunk,seed", [
@@ -151,7 +167,7 @@ def test_ignored_rows_do_not_matter(dev):
 
 def test_component_workload_full(dev):
     # B=4, S=1024, H=512, V=16000 with 5% ignored, default (5%) plan
-    check_full(wl.make_inputs(wl.WORKLOADS["component"]), dev)
+    check_full(wl.make_inputs(wl.WORKLOADS["component"]), dev, case="component")
 
 
 # --------------------------------------------------------------------------
@@ -165,10 +181,17 @@ def test_bad_target_status(dev):
     h, w, t = to_device(p, dev)
     out = flce.fwd_bwd(h, w, t)
     assert flce.query_status(out["workspace"]) == flce.FLCE_EBADTARGET
+    assert math.isnan(float(out["loss"].item()))        # a failed call reports a NaN loss
     p["targets"][17] = -7
     h, w, t = to_device(p, dev)
     out = flce.fwd_bwd(h, w, t)
     assert flce.query_status(out["workspace"]) == flce.FLCE_EBADTARGET
+    assert math.isnan(float(out["loss"].item()))
+    p["targets"][17] = 3                                 # the same workspace, a good call: status cleared
+    h, w, t = to_device(p, dev)
+    out = flce.fwd_bwd(h, w, t, workspace=out["workspace"])
+    assert flce.query_status(out["workspace"]) == flce.FLCE_OK
+    assert math.isfinite(float(out["loss"].item()))
 
 
 def test_timeout_path_returns(dev):
@@ -180,16 +203,86 @@ def test_timeout_path_returns(dev):
     check_full(wl.random_problem(64, 32, 100, seed=15), dev)          # context still healthy
 
 
+W_TMEM_FULL = 10   # wait site: an epilogue waiting for its accumulator (flce_query_stall)
+
+
+def test_gemm_pipeline_timeout(dev):
+    # The tcgen05 GEMM's own failure path: the armed launch (the first logits
+    # launch of the call) withholds the accumulator-ready signal of the first
+    # tile of every CTA pair, the epilogues' bounded waits run out after 50 ms,
+    # and every CTA aborts (drains its copies, waits for its MMAs, frees TMEM).
+    flce = _flce()
+    p = wl.random_problem(300, 64, 512, seed=16)
+    h, w, t = to_device(p, dev)
+    flce.debug_arm_stall(50_000_000)
+    out = flce.fwd_bwd(h, w, t)
+    assert flce.query_status(out["workspace"]) == flce.FLCE_ETIMEOUT
+    st = flce.query_stall(out["workspace"])
+    assert st["site"] == W_TMEM_FULL and st["count"] >= 1, st
+    assert math.isnan(float(out["loss"].item()))
+    # the same workspace and context: the next call is normal
+    out = flce.fwd_bwd(h, w, t, workspace=out["workspace"])
+    assert flce.query_status(out["workspace"]) == flce.FLCE_OK
+    assert flce.query_stall(out["workspace"])["site"] == 0
+    check_full(p, dev)
+
+
+def test_grad_weight_bf16(dev):
+    # FLCE_GW_BF16: the same fp32 accumulation, rounded once to bf16 at the end
+    flce = _flce()
+    import torch
+    p = wl.random_problem(1000, 200, 1000, seed=17, ignore_frac=0.1)
+    h, w, t = to_device(p, dev)
+    a = flce.fwd_bwd(h, w, t, chunk_rows=128)
+    b = flce.fwd_bwd(h, w, t, chunk_rows=128, grad_weight_dtype=torch.bfloat16)
+    assert flce.query_status(b["workspace"]) == flce.FLCE_OK
+    assert b["grad_weight"].dtype == torch.bfloat16
+    assert torch.equal(b["grad_weight"], a["grad_weight"].to(torch.bfloat16))
+    assert torch.equal(a["grad_hidden"], b["grad_hidden"]) and torch.equal(a["loss"], b["loss"])
+    ref = flce_oracle(p["hidden"], p["weight"], p["targets"])
+    e = frob_rel(b["grad_weight"].double().cpu().numpy(), ref["grad_weight"])
+    assert e <= GRAD_FROB_RTOL
+    report("grad_weight_bf16", grad_weight=e)
+
+
 # --------------------------------------------------------------------------
 # full-size workloads, default plan (the benchmark's launch configuration)
 # --------------------------------------------------------------------------
 
-def _sampled(name, dev, n_rows=24, vocab_rows=None, reduce=None):
+def _vocab_rows(p, V, n_min=32):
+    """Vocabulary rows of grad_weight to compare with the oracle: the first and
+    last rows, both sides of 128-column part and 256-row tile boundaries, the
+    last (possibly partial) 256-row tile, the 8 most frequent targets, and
+    seeded random rows up to n_min."""
+    t = p["targets"]
+    freq = np.bincount(t[t != -100], minlength=V)
+    rows = {0, 1, V - 2, V - 1}
+    for b in (128, 256, 384, 512, (V // 2) // 128 * 128):
+        rows.update(v for v in (b - 1, b) if 0 <= v < V)
+    last_tile = (V - 1) // 256 * 256
+    rows.update(range(max(last_tile, V - 8), V))      # every row of a partial last tile (V=256007: 7 rows)
+    rows.update(int(v) for v in np.argsort(-freq, kind="stable")[:8])
+    rng = np.random.default_rng(V)
+    while len(rows) < n_min:
+        rows.add(int(rng.integers(0, V)))
+    return np.array(sorted(rows))
+
+
+def _sampled(name, dev, n_rows=24, reduce=None):
+    """One call of the default plan (the benchmark's launch configuration) at a
+    full-size workload, compared with the fp64 oracle on:
+      * the total loss (every valid row's log-sum-exp from the oracle),
+      * >= 32 rows of grad_weight (every valid row contributes to each),
+      * grad_hidden and the per-row loss on the first and last valid row of
+        every token chunk plus seeded random rows and two ignored rows,
+    plus two properties that hold at any size."""
     flce = _flce()
     import torch
     w_ = wl.WORKLOADS[name] if reduce is None else wl.WORKLOADS[name].with_shape(**reduce)
     p = wl.make_inputs(w_)
     h, w, t = to_device(p, dev)
+    N, H, V = w_.N, w_.H, w_.V
+    C = flce.plan(N, H, V, flce.workspace_bytes(N, H, V))["chunk_rows"]
     out = flce.fwd_bwd(h, w, t, row_loss=True)
     assert flce.query_status(out["workspace"]) == flce.FLCE_OK
     nv = int(out["n_valid"].item())
@@ -197,17 +290,23 @@ def _sampled(name, dev, n_rows=24, vocab_rows=None, reduce=None):
     rng = np.random.default_rng(123)
     valid = np.nonzero(p["targets"] != -100)[0]
     ign = np.nonzero(p["targets"] == -100)[0]
-    rows = np.sort(np.concatenate([rng.choice(valid, size=min(n_rows, valid.size), replace=False),
-                                   ign[:2], valid[:1], valid[-1:]]))
+    edges = [valid[c0] for c0 in range(0, valid.size, C)] + \
+            [valid[min(c0 + C, valid.size) - 1] for c0 in range(0, valid.size, C)]
+    rows = np.unique(np.concatenate([rng.choice(valid, size=min(n_rows, valid.size), replace=False),
+                                     ign[:2], np.array(edges, dtype=np.int64)]))
     W64 = decode_bf16(p["weight"])
     ref = oracle_rows(p["hidden"][rows], p["weight"], p["targets"][rows], nv, weight_f64=W64)
     rl = out["row_loss"][torch.from_numpy(rows).to(dev)].cpu().double().numpy()
-    assert np.max(np.abs(rl - ref["row_loss"])) <= LOSS_RTOL * np.abs(ref["row_loss"]).max()
+    e_rl = np.max(np.abs(rl - ref["row_loss"])) / np.abs(ref["row_loss"]).max()
+    assert e_rl <= LOSS_RTOL
     gh = gh_np(out["grad_hidden"][torch.from_numpy(rows).to(dev)])
-    assert frob_rel(gh, ref["grad_hidden"]) <= GRAD_FROB_RTOL
+    e_gh = frob_rel(gh, ref["grad_hidden"])
+    assert e_gh <= GRAD_FROB_RTOL
     for i, r in enumerate(rows):
         if p["targets"][r] != -100:
-            assert frob_rel(gh[i], ref["grad_hidden"][i]) <= 3 * GRAD_FROB_RTOL
+            assert frob_rel(gh[i], ref["grad_hidden"][i]) <= 3 * GRAD_FROB_RTOL, r
+        else:
+            assert not gh[i].any()
     gw = out["grad_weight"]
     # softmax rows sum to one, so the columns of grad_weight sum to zero
     col = gw.double().sum(dim=0)
@@ -216,21 +315,26 @@ def _sampled(name, dev, n_rows=24, vocab_rows=None, reduce=None):
     a = (out["grad_hidden"].double() * h.double()).sum().item()
     b = (gw.double() * w.double()).sum().item()
     assert abs(a - b) <= GRAD_FROB_RTOL * max(abs(a), abs(b)), (a, b)
-    if vocab_rows is not None:
-        lse = lse_all_rows(p["hidden"], p["weight"], p["targets"], weight_f64=W64)
-        vr = np.array(vocab_rows)
-        ew = grad_weight_rows(p["hidden"], p["weight"], p["targets"], lse, vr, weight_f64=W64)
-        got = gw[torch.from_numpy(vr).to(dev)].cpu().double().numpy()
-        assert frob_rel(got, ew) <= GRAD_FROB_RTOL
-        ref_loss = float(np.nansum(lse - np.where(p["targets"] != -100,
-                                                   (decode_bf16(p["hidden"]) * W64[np.clip(p["targets"], 0, None)]).sum(1),
-                                                   np.nan)) / nv)
-        assert loss_rel(float(out["loss"].item()), ref_loss) <= LOSS_RTOL
+    # total loss and grad_weight rows against the oracle (needs every row's lse)
+    lse = lse_all_rows(p["hidden"], p["weight"], p["targets"], weight_f64=W64)
+    vr = _vocab_rows(p, V)
+    assert vr.size >= 32
+    ew = grad_weight_rows(p["hidden"], p["weight"], p["targets"], lse, vr, weight_f64=W64)
+    got = gw[torch.from_numpy(vr).to(dev)].cpu().double().numpy()
+    e_gw = frob_rel(got, ew)
+    assert e_gw <= GRAD_FROB_RTOL
+    X64 = decode_bf16(p["hidden"][valid])
+    zt = (X64 * W64[p["targets"][valid]]).sum(axis=1)
+    ref_loss = float((lse[valid] - zt).sum()) / nv
+    e_loss = loss_rel(float(out["loss"].item()), ref_loss)
+    assert e_loss <= LOSS_RTOL
+    report(name, loss=e_loss, row_loss=e_rl, grad_hidden_rows=e_gh, grad_weight_rows=e_gw,
+           n_grad_hidden_rows=rows.size, n_grad_weight_rows=vr.size, chunk_rows=C)
     return out
 
 
 def test_full_model_workload(dev):
-    _sampled("full_model", dev, vocab_rows=[0, 1, 7, 15999])
+    _sampled("full_model", dev)
 
 
 def test_llama3_head_workload(dev):
@@ -249,4 +353,4 @@ def test_large_vocab_tail_workload(dev):
 def test_full_vocab_reduced_tokens(dev, name, N):
     # full H and V of the big workloads, fewer tokens so the oracle runs whole;
     # 128-row chunks exercise the fp32 grad_weight accumulation at full V
-    check_full(wl.make_inputs(wl.WORKLOADS[name].with_shape(N=N)), dev, chunk_rows=128)
+    check_full(wl.make_inputs(wl.WORKLOADS[name].with_shape(N=N)), dev, chunk_rows=128, case=f"{name}_N{N}")
