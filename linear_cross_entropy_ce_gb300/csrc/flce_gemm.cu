@@ -50,15 +50,22 @@ constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 columns of 
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SLICE_COLS = 16;              // fp32 columns per staged output slice (64 B rows)
 constexpr int STG_BYTES = BM * SLICE_COLS * 4;   // one 128 x 16 fp32 slice: 8 KB
-constexpr int EPI_GROUPS = 2;               // epilogue warpgroups, one per 128-column half
-constexpr int GROUP_COLS = BN / EPI_GROUPS;
+// Two epilogue sets, one per TMEM accumulator, so that the epilogues of two
+// consecutive tiles run at once (tiles with few K blocks are bound by their
+// epilogue); each set has two warpgroups, one per 128-column half.
+constexpr int EPI_SETS = 2;
+constexpr int SET_GROUPS = 2;
+constexpr int EPI_GROUPS = EPI_SETS * SET_GROUPS;
+constexpr int GROUP_COLS = BN / SET_GROUPS;
 constexpr int GROUP_THREADS = 128;
+constexpr int SET_THREADS = SET_GROUPS * GROUP_THREADS;
 constexpr int EPI_THREADS = EPI_GROUPS * GROUP_THREADS;
+constexpr int EPI_WARPS = EPI_THREADS / 32;
 constexpr int NUM_THREADS = 64 + EPI_THREADS;   // warp 0 TMA, warp 1 MMA, then the epilogue warps
 constexpr int SCHED_SLOTS = 4;
 constexpr int SHORT_TILE_KB = 32;           // tiles with at most this many K blocks claim their successor early
-constexpr uint32_t EPI_BAR_ALL = 1;         // named barrier of all epilogue warps
-constexpr uint32_t EPI_BAR_GROUP = 2;       // + warpgroup index: per-warpgroup named barrier
+constexpr uint32_t EPI_BAR_SET = 1;         // + set index: named barrier of one epilogue set
+constexpr uint32_t EPI_BAR_GROUP = 1 + EPI_SETS;   // + warpgroup index: per-warpgroup named barrier
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int MN_BLOCK_BYTES = 64 * 128;    // 64 K rows x 128 B (64 bf16 along M or N)
 constexpr uint16_t PAIR_MASK = 0x3;
@@ -68,7 +75,7 @@ struct Ctl {
   uint64_t full[STAGES_LOGITS];  // CTA 0: both CTAs' loads of a stage landed
   uint64_t empty[STAGES_LOGITS]; // each CTA: the pair's MMAs released the stage
   uint64_t tfull[2];           // each CTA: accumulator ready
-  uint64_t tempty[2];          // CTA 0: both CTAs' epilogues drained the accumulator
+  uint64_t tempty[2];          // CTA 0: every warp of the accumulator's epilogue set in both CTAs has read it
   uint64_t sfull[SCHED_SLOTS]; // each CTA: a tile id is in sunit
   uint64_t sempty[SCHED_SLOTS];// CTA 0: every reader of the slot is done
   uint64_t mma_done;
@@ -78,14 +85,16 @@ struct Ctl {
 };
 
 constexpr int CTL_BYTES = ((sizeof(Ctl) + 255) / 256) * 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * EPI_GROUPS * STG_BYTES + CTL_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_GROUPS * STG_BYTES + CTL_BYTES;   // one staging buffer per warpgroup
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(STAGES_LOGITS * STAGE_BYTES <= STAGES * STAGE_BYTES + 2 * EPI_GROUPS * STG_BYTES,
+static_assert(STAGES_LOGITS * STAGE_BYTES <= STAGES * STAGE_BYTES + EPI_GROUPS * STG_BYTES,
               "the extra logits stages fit in the epilogue staging area");
 
-// Readers of a scheduler slot: in CTA 0 the MMA lane and its epilogue
-// threads, in CTA 1 the TMA lane and its epilogue threads.
-constexpr uint32_t SCHED_READERS = 2 * (1 + EPI_THREADS);
+// Readers of a scheduler slot, one arrival per warp: in CTA 0 the MMA lane
+// and the epilogue warps, in CTA 1 the TMA lane and the epilogue warps.
+constexpr uint32_t SCHED_READERS = 2 * (1 + EPI_WARPS);
+// Arrivals that free an accumulator: every warp of its set, in both CTAs.
+constexpr uint32_t TEMPTY_ARRIVALS = 2 * (SET_THREADS / 32);
 
 // Bounded wait on an mbarrier phase.  Gives up (returning false) when the
 // CTA's abort flag is raised by another role, or after timeout_ns, in which
@@ -354,19 +363,22 @@ __device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s,
 // The warpgroup's 128 x 128 fp32 accumulator block -> 16-column slices ->
 // shared memory (64-byte rows, 64-byte swizzle: chunk g of row r sits at
 // g ^ ((r >> 1) & 3), conflict-free) -> TMA store (reduce == false) or TMA
-// reduce-add into `map` at (h, row0).  Two staging buffers per warpgroup
-// alternate; `leader` (one thread of the warpgroup) owns the bulk groups.
+// reduce-add into `map` at (h, row0).  One staging buffer per warpgroup (the
+// four warpgroups keep the TMA unit busy between them); `leader` (one thread
+// of the warpgroup) owns the bulk groups.  The next slice's TMEM load is
+// issued before the wait for the buffer.
 __device__ __forceinline__ void block_to_global(const CUtensorMap* map, int ncols_total, int h0, int row0,
                                                 bool reduce, uint32_t tbase, int r, bool leader, uint32_t bar,
-                                                uint8_t* stg, uint32_t& stg_count) {
+                                                uint8_t* buf) {
+  const int left = ncols_total - h0;
+  const int nsl = left <= 0 ? 0 : min(GROUP_COLS / SLICE_COLS, (left + SLICE_COLS - 1) / SLICE_COLS);
+  if (nsl == 0) return;   // uniform over the warpgroup
+  float v[SLICE_COLS];
+  ptx::tmem_ld16(tbase, v);
 #pragma unroll 1
-  for (int j = 0; j < GROUP_COLS / SLICE_COLS; ++j) {
+  for (int j = 0; j < nsl; ++j) {
     const int h = h0 + j * SLICE_COLS;
-    if (h >= ncols_total) break;  // uniform over the warpgroup
-    float v[SLICE_COLS];
-    ptx::tmem_ld16(tbase + j * SLICE_COLS, v);
-    uint8_t* buf = stg + (stg_count & 1u) * STG_BYTES;
-    if (leader) ptx::bulk_wait_read_1();          // the store that last used `buf` has read it
+    if (leader) ptx::bulk_wait_read_0();          // the previous slice's store has read the buffer
     ptx::named_bar_sync(bar, GROUP_THREADS);
     uint8_t* row = buf + r * (SLICE_COLS * 4);
 #pragma unroll
@@ -382,7 +394,7 @@ __device__ __forceinline__ void block_to_global(const CUtensorMap* map, int ncol
         ptx::tma_store_2d(map, buf, h, row0);
       ptx::bulk_commit();
     }
-    ++stg_count;
+    if (j + 1 < nsl) ptx::tmem_ld16(tbase + (j + 1) * SLICE_COLS, v);
   }
 }
 
@@ -391,10 +403,10 @@ __device__ __forceinline__ void block_to_global(const CUtensorMap* map, int ncol
 // the finished fp32 rows into bf16 grad_hidden rows.  Each warpgroup orders
 // its own column half.  Returns false on abort.
 __device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* maps, const Shape& s,
-                                             const Unit& t, int row0, int col0, int grp, uint32_t rank,
+                                             const Unit& t, int row0, int col0, int half_idx, uint32_t rank,
                                              uint32_t tbase, int r, bool leader, uint32_t bar, uint8_t* stg,
-                                             uint32_t& stg_count, Ctl* ctl) {
-  int* flag = a.flags + 4 * t.ntile + 2 * static_cast<int>(rank) + grp;
+                                             Ctl* ctl) {
+  int* flag = a.flags + 4 * t.ntile + 2 * static_cast<int>(rank) + half_idx;
   bool ok = true;
   if (leader && t.split > 0) {
     ok = wait_flag(flag, t.split, ctl, a.timeout_ns, const_cast<int*>(a.hdr));
@@ -402,7 +414,7 @@ __device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* 
   }
   if (!ptx::named_bar_and(bar, GROUP_THREADS, ok)) return false;
   const int h0 = t.n0 + col0;
-  block_to_global(&maps->dx, a.H, h0, row0, t.split > 0, tbase, r, leader, bar, stg, stg_count);
+  block_to_global(&maps->dx, a.H, h0, row0, t.split > 0, tbase, r, leader, bar, stg);
   if (leader) {
     ptx::bulk_wait_all();                 // this part has landed in global memory
     ptx::fence_proxy_async_global();
@@ -441,7 +453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg = smem + STAGES * STAGE_BYTES;
-  Ctl* ctl = reinterpret_cast<Ctl*>(stg + 2 * EPI_GROUPS * STG_BYTES);
+  Ctl* ctl = reinterpret_cast<Ctl*>(stg + EPI_GROUPS * STG_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ptx::cluster_ctarank();
   const bool lead = rank == 0;
@@ -467,7 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ctl->tfull[i], 1);
-      ptx::mbar_init(&ctl->tempty[i], 2 * EPI_THREADS);   // both CTAs' epilogue threads
+      ptx::mbar_init(&ctl->tempty[i], TEMPTY_ARRIVALS);
     }
     for (int i = 0; i < SCHED_SLOTS; ++i) {
       ptx::mbar_init(&ctl->sfull[i], 1);
@@ -612,25 +624,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ptx::umma_commit_pair(&ctl->mma_done, 0x1);
     wait_phase(&ctl->mma_done, 0, ctl, to, false, hdr, W_MMA_DONE);
   } else if (warp >= 2) {
-    // ---------------- epilogue (both CTAs: 128 rows each, two warpgroups) ----------------
+    // ---------------- epilogue (both CTAs: 128 rows each) ----------------
+    // Set e drains accumulator e, i.e. every other tile of the pair; its two
+    // warpgroups take one 128-column half each.  Every epilogue warp reads
+    // every scheduler slot, so both sets follow the same tile sequence.
     const int q = warp & 3;                   // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;              // accumulator row within this CTA's half
-    const int grp = (warp - 2) / 4;           // warpgroup: column half of the tile
-    const int col0 = grp * GROUP_COLS;
+    const int grp = (warp - 2) / 4;           // warpgroup
+    const int set = grp / SET_GROUPS;         // the accumulator this warpgroup drains
+    const int half_idx = grp % SET_GROUPS;    // its column half of the tile
+    const int col0 = half_idx * GROUP_COLS;
     const bool leader = ((warp - 2) & 3) == 0 && lane == 0;
     const uint32_t gbar = EPI_BAR_GROUP + static_cast<uint32_t>(grp);
-    uint8_t* gstg = stg + grp * 2 * STG_BYTES;
+    const uint32_t sbar = EPI_BAR_SET + static_cast<uint32_t>(set);
+    uint8_t* gstg = stg + grp * STG_BYTES;
     const uint32_t sempty0 = ptx::map_to_rank(&ctl->sempty[0], 0);
-    const uint32_t tempty0 = ptx::map_to_rank(&ctl->tempty[0], 0);
-    uint32_t acc = 0, acc_phase = 0, sslot = 0, sphase = 0, stg_count = 0;
+    const uint32_t tempty_mine = ptx::map_to_rank(&ctl->tempty[set], 0);
+    uint32_t seq = 0, acc_phase = 0, sslot = 0, sphase = 0;
     for (;;) {
-      // every wait is followed by a vote so that all epilogue threads leave together
+      // every wait is followed by a vote so that all threads of the set leave together
       bool ok = wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_EPI, sslot << 24);
-      if (!ptx::named_bar_and(EPI_BAR_ALL, EPI_THREADS, ok)) break;
+      if (!ptx::named_bar_and(sbar, SET_THREADS, ok)) break;
       const int u = ctl->sunit[sslot];
-      ptx::mbar_arrive_remote(sempty0 + sslot * 8u);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(sempty0 + sslot * 8u);
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
+      if ((seq++ & 1u) != static_cast<uint32_t>(set)) continue;   // the other set's tile
       const Unit t = decode_unit(a, s, u);
       if (t.kind == U_DW && a.accumulate && a.pf_threads) {
         // this thread's row of the grad_weight tile (128 fp32 = 4 lines) into
@@ -644,10 +664,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             if (t.n0 + col0 + q4 * 32 < a.H) ptx::prefetch_l2(gp + q4 * 32);
         }
       }
-      ok = wait_phase(&ctl->tfull[acc], acc_phase, ctl, to, true, hdr, W_TMEM_FULL, u | (acc << 24));
-      if (!ptx::named_bar_and(EPI_BAR_ALL, EPI_THREADS, ok)) break;
+      ok = wait_phase(&ctl->tfull[set], acc_phase, ctl, to, true, hdr, W_TMEM_FULL, u | (set << 24));
+      if (!ptx::named_bar_and(sbar, SET_THREADS, ok)) break;
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + col0;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + set * BN + col0;
       const int row0 = t.m0 + half;
       bool cont = true;
       if (t.kind == U_LOGITS)
@@ -655,15 +675,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       else if (t.kind == U_DX && a.splits == 1)
         epi_dx_direct(a, s, t, row0, col0, tbase, r);
       else if (t.kind == U_DX)
-        cont = epi_dx_split(a, &maps, s, t, row0, col0, grp, rank, tbase, r, leader, gbar, gstg, stg_count, ctl);
+        cont = epi_dx_split(a, &maps, s, t, row0, col0, half_idx, rank, tbase, r, leader, gbar, gstg, ctl);
       else
-        block_to_global(&maps.out, a.H, t.n0 + col0, row0, a.accumulate != 0, tbase, r, leader, gbar, gstg,
-                        stg_count);
+        block_to_global(&maps.out, a.H, t.n0 + col0, row0, a.accumulate != 0, tbase, r, leader, gbar, gstg);
       ptx::tc_fence_before();
-      ptx::mbar_arrive_remote(tempty0 + acc * 8u);
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
-      if (!ptx::named_bar_and(EPI_BAR_ALL, EPI_THREADS, cont)) break;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(tempty_mine);   // this warp's lanes of the accumulator are read
+      acc_phase ^= 1u;
+      if (!ptx::named_bar_and(sbar, SET_THREADS, cont)) break;
     }
     if (leader) ptx::bulk_wait_all();
   }
