@@ -391,9 +391,7 @@ flce_status run(const Job& j) {
          make_map(&bm.out, gwacc, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B) &&
          make_map(&bm.pf, gwacc, H, V, static_cast<unsigned long long>(H) * 4, BN, BM,
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         (!dxacc || make_map(&bm.dx, dxacc, H, p.C, static_cast<unsigned long long>(H) * 4, 16, BM,
-                             CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B));
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return FLCE_ECUDA;
 
   const int reduce_sum = (j.flags & FLCE_REDUCE_SUM) ? 1 : 0;

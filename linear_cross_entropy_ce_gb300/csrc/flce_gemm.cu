@@ -398,31 +398,69 @@ __device__ __forceinline__ void block_to_global(const CUtensorMap* map, int ncol
   }
 }
 
+// One warp's 32 accumulator rows x 128 fp32 columns -> dst rows [row0,
+// row0 + 32), columns [h0, h0 + 128) of a [rows][ncols] fp32 array, 16
+// columns at a time: a tcgen05 load gives each thread one row, the slice is
+// turned around in the warp's own 2 KB of shared memory (64-byte rows,
+// 16-byte chunks swizzled so that the row writes and the transposed reads are
+// both conflict-free), and each vector access of the warp then covers 8 rows
+// x 64 contiguous bytes: st.global.v4 (store) or red.global.add.v4.f32
+// (accumulate, performed at L2).  For one SM alone this moves the block
+// about twice as fast as TMA stores or reduce-adds of 16 x 128 boxes, which
+// is what the ordered chain of grad_hidden splits needs; with every SM
+// updating grad_weight at once the TMA reduce-add is faster (the
+// Llama-3-8B-head backward is 9% slower with this path), so grad_weight
+// keeps block_to_global.  Rows >= nrows and columns >= ncols are skipped.
+__device__ __forceinline__ void warp_block_to_global(float* dst, int nrows, int ncols, int h0, int row0, bool reduce,
+                                                     uint32_t tbase, int lane, uint8_t* wbuf) {
+  const int left = ncols - h0;
+  const int nsl = left <= 0 ? 0 : min(GROUP_COLS / SLICE_COLS, (left + SLICE_COLS - 1) / SLICE_COLS);
+  uint8_t* wrow = wbuf + lane * (SLICE_COLS * 4);
+  const int wsw = (lane >> 1) & 3;
+  const int c = lane & 3;                   // the 16-byte chunk this thread moves
+#pragma unroll 1
+  for (int j = 0; j < nsl; ++j) {           // uniform over the warp
+    float v[SLICE_COLS];
+    ptx::tmem_ld16(tbase + j * SLICE_COLS, v);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      *reinterpret_cast<float4*>(wrow + ((g ^ wsw) << 4)) = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    __syncwarp();
+    const int h = h0 + j * SLICE_COLS + 4 * c;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int rr = (lane >> 2) + 8 * p;
+      const float4 x = *reinterpret_cast<const float4*>(wbuf + rr * (SLICE_COLS * 4) + ((c ^ ((rr >> 1) & 3)) << 4));
+      if (row0 + rr < nrows && h < ncols) {
+        float* d = dst + static_cast<size_t>(row0 + rr) * ncols + h;
+        if (reduce)
+          ptx::red_add_v4(d, x);
+        else
+          *reinterpret_cast<float4*>(d) = x;
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // dX unit of a split vocabulary: split 0 stores its fp32 part, split k waits
 // until split k-1 has landed and reduce-adds onto it, the last split turns
 // the finished fp32 rows into bf16 grad_hidden rows.  Each warpgroup orders
 // its own column half.  Returns false on abort.
-__device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* maps, const Shape& s,
-                                             const Unit& t, int row0, int col0, int half_idx, uint32_t rank,
-                                             uint32_t tbase, int r, bool leader, uint32_t bar, uint8_t* stg,
-                                             Ctl* ctl) {
+__device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const Shape& s, const Unit& t, int row0, int col0,
+                                             int half_idx, uint32_t rank, uint32_t tbase, int r, int q, int lane,
+                                             bool leader, uint32_t bar, uint8_t* wbuf, Ctl* ctl) {
   int* flag = a.flags + 4 * t.ntile + 2 * static_cast<int>(rank) + half_idx;
   bool ok = true;
-  if (leader && t.split > 0) {
-    ok = wait_flag(flag, t.split, ctl, a.timeout_ns, const_cast<int*>(a.hdr));
-    ptx::fence_proxy_async_global();
-  }
+  if (leader && t.split > 0) ok = wait_flag(flag, t.split, ctl, a.timeout_ns, const_cast<int*>(a.hdr));
   if (!ptx::named_bar_and(bar, GROUP_THREADS, ok)) return false;
   const int h0 = t.n0 + col0;
-  block_to_global(&maps->dx, a.H, h0, row0, t.split > 0, tbase, r, leader, bar, stg);
-  if (leader) {
-    ptx::bulk_wait_all();                 // this part has landed in global memory
-    ptx::fence_proxy_async_global();
-    __threadfence();
-    ptx::st_release_gpu(flag, t.split + 1);
-  }
+  float* acc = const_cast<float*>(a.dxacc);
+  warp_block_to_global(acc, a.C, a.H, h0, row0 + q * 32, t.split > 0, tbase, lane, wbuf);
+  __threadfence();                          // this part is in global memory before the flag moves on
+  ptx::named_bar_sync(bar, GROUP_THREADS);
+  if (leader) ptx::st_release_gpu(flag, t.split + 1);
   if (t.split == a.splits - 1) {
-    ptx::named_bar_sync(bar, GROUP_THREADS);
     const int grow = row0 + r;
     if (grow < s.Cl) {
       const long long tok = a.idx[a.c0 + grow];
@@ -434,8 +472,8 @@ __device__ __forceinline__ bool epi_dx_split(const GemmArgs& a, const GemmMaps* 
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           if (h + 4 * g < a.H) {
-            const float4 q = __ldcg(reinterpret_cast<const float4*>(src + h + 4 * g));
-            v[4 * g] = q.x; v[4 * g + 1] = q.y; v[4 * g + 2] = q.z; v[4 * g + 3] = q.w;
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + h + 4 * g));
+            v[4 * g] = x.x; v[4 * g + 1] = x.y; v[4 * g + 2] = x.z; v[4 * g + 3] = x.w;
           } else {
             v[4 * g] = v[4 * g + 1] = v[4 * g + 2] = v[4 * g + 3] = 0.f;
           }
@@ -495,7 +533,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       ptx::tma_prefetch_desc(&maps.b1);
       ptx::tma_prefetch_desc(&maps.out);
       ptx::tma_prefetch_desc(&maps.pf);
-      if (a.splits > 1) ptx::tma_prefetch_desc(&maps.dx);
     }
   }
   if (warp == 1) {
@@ -637,7 +674,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const bool leader = ((warp - 2) & 3) == 0 && lane == 0;
     const uint32_t gbar = EPI_BAR_GROUP + static_cast<uint32_t>(grp);
     const uint32_t sbar = EPI_BAR_SET + static_cast<uint32_t>(set);
-    uint8_t* gstg = stg + grp * STG_BYTES;
+    uint8_t* gstg = stg + grp * STG_BYTES;                      // this warpgroup's staging buffer, and
+    uint8_t* wbuf = stg + (warp - 2) * (32 * SLICE_COLS * 4);   // the same bytes as four per-warp 2 KB buffers
     const uint32_t sempty0 = ptx::map_to_rank(&ctl->sempty[0], 0);
     const uint32_t tempty_mine = ptx::map_to_rank(&ctl->tempty[set], 0);
     uint32_t seq = 0, acc_phase = 0, sslot = 0, sphase = 0;
@@ -675,7 +713,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       else if (t.kind == U_DX && a.splits == 1)
         epi_dx_direct(a, s, t, row0, col0, tbase, r);
       else if (t.kind == U_DX)
-        cont = epi_dx_split(a, &maps, s, t, row0, col0, half_idx, rank, tbase, r, leader, gbar, gstg, ctl);
+        cont = epi_dx_split(a, s, t, row0, col0, half_idx, rank, tbase, r, q, lane, leader, gbar, wbuf, ctl);
       else
         block_to_global(&maps.out, a.H, t.n0 + col0, row0, a.accumulate != 0, tbase, r, leader, gbar, gstg);
       ptx::tc_fence_before();

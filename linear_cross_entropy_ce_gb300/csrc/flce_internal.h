@@ -76,10 +76,9 @@ struct GemmArgs {
 // Tensor maps of one launch.  LOGITS: a0 = Xc (K-major), b0 = W (K-major).
 // BWD: a0 = dz (K-major), b0 = W (MN-major), a1 = dz (MN-major view),
 // b1 = Xc (MN-major), out = grad_weight (fp32, store / reduce-add of 16 x 128
-// slices), dx = the fp32 grad_hidden split accumulator (same slices),
-// pf = grad_weight again with a 256 x 128 box for L2 prefetches.
+// slices), pf = grad_weight again with a 256 x 128 box for L2 prefetches.
 struct GemmMaps {
-  CUtensorMap a0, b0, a1, b1, out, dx, pf;   // pf: grad_weight, 256 x 128 box, L2 prefetch
+  CUtensorMap a0, b0, a1, b1, out, pf;
 };
 
 int gemm_smem_bytes();

@@ -140,6 +140,13 @@ __device__ __forceinline__ void ld_global_v8_cs(const void* p, uint32_t (&r)[8])
                : "l"(reinterpret_cast<uint64_t>(p)));
 }
 
+// *p += x for four fp32 lanes, performed at L2 (no value returned); `p` 16-byte aligned.
+__device__ __forceinline__ void red_add_v4(float* p, float4 x) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(reinterpret_cast<uint64_t>(p)), "f"(x.x),
+               "f"(x.y), "f"(x.z), "f"(x.w)
+               : "memory");
+}
+
 // Plain (LSU) prefetch of the 128-byte line holding `p` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
