@@ -282,8 +282,11 @@ flce_status flce_selftest_timeout(void* workspace, uint64_t timeout_ns,
  * budgets).  The pages have no counterpart: it is a deployment variant of
  * flce_fwd_bwd with the same arguments, outputs and tolerances.
  *   Scratch: a static device array of FLCE_NOALLOC_WORKSPACE_BYTES (64 MiB)
- *     inside the library, held by every GPU that loads the library until the
- *     process exits.  The call itself allocates nothing.
+ *     inside the library.  A GPU holds it from the moment it loads the
+ *     array's module until the process exits: with CUDA's lazy module loading
+ *     (the default under PyTorch) that is this entry point's first call on the
+ *     device, with eager loading the loading of the library.  The call itself
+ *     allocates nothing.
  *   Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -294,7 +297,8 @@ flce_status flce_selftest_timeout(void* workspace, uint64_t timeout_ns,
  *     on the GPU (other streams, other threads) race and give wrong results;
  *     serialise them.  The array needs no clearing between calls.
  *   Device-side status (bad targets, time-outs) is written into the array
- *     and cannot be read back through flce_query_status.
+ *     and cannot be read back through flce_query_status; such a call writes
+ *     a NaN loss.
  */
 #define FLCE_NOALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 flce_status flce_fwd_bwd_noalloc(const void* hidden, const void* weight,
