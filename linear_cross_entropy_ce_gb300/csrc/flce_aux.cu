@@ -63,44 +63,56 @@ struct AddOp {
 
 // ---------------------------------------------------------------------------
 constexpr int PREP_THREADS = 1024;
+constexpr int PREP_WARPS = PREP_THREADS / 32;
 
+__device__ __forceinline__ bool target_valid(int x, int ii, int V) { return x != ii && x >= 0 && x < V; }
+
+// One block: pass 1 counts the valid targets (coalesced reads); pass 2 walks
+// the targets in tiles of 1024 and places every row with a warp ballot and a
+// scan of the 32 warp counts: valid rows in order first, then the others in
+// order.
 __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restrict__ t, long long N, int V,
                                                              int ii, int* hdr, int* __restrict__ idx,
                                                              int* n_valid_out, int* counters,
                                                              long long n_counters) {
-  __shared__ int cnt[PREP_THREADS];
+  __shared__ int red[PREP_WARPS];
+  __shared__ int wsum[PREP_WARPS];
   __shared__ int bad;
-  const int tid = threadIdx.x;
-  const long long seg = (N + PREP_THREADS - 1) / PREP_THREADS;
-  const long long b = tid * seg;
-  const long long e = b + seg < N ? b + seg : N;
-  int c = 0, mybad = 0;
-  for (long long i = b; i < e; ++i) {
-    const int x = t[i];
-    if (x != ii) {
-      if (x >= 0 && x < V) ++c;
-      else mybad = 1;
-    }
-  }
+  const int tid = threadIdx.x, lane = tid % 32, w = tid / 32;
   if (tid == 0) bad = 0;
   for (long long i = tid; i < n_counters; i += PREP_THREADS) counters[i] = 0;  // GEMM tile counters, split flags
-  cnt[tid] = c;
-  __syncthreads();
-  if (mybad) bad = 1;
-  // inclusive scan of the per-thread counts (Hillis-Steele)
-  for (int off = 1; off < PREP_THREADS; off <<= 1) {
-    const int add = tid >= off ? cnt[tid - off] : 0;
-    __syncthreads();
-    cnt[tid] += add;
-    __syncthreads();
-  }
-  const int total = cnt[PREP_THREADS - 1];
-  int pos = cnt[tid] - c;                                      // valid rows before b
-  long long ipos = total + ((b < N ? b : N) - pos);           // other rows go after all valid ones
-  for (long long i = b; i < e; ++i) {
+  int c = 0, mybad = 0;
+  for (long long i = tid; i < N; i += PREP_THREADS) {
     const int x = t[i];
-    if (x != ii && x >= 0 && x < V) idx[pos++] = static_cast<int>(i);
-    else idx[ipos++] = static_cast<int>(i);
+    if (target_valid(x, ii, V)) ++c;
+    else if (x != ii) mybad = 1;
+  }
+  const int total = block_reduce(c, AddOp(), 0, red);
+  if (mybad) bad = 1;
+  const unsigned lt = (1u << lane) - 1u;
+  long long done = 0;   // valid rows in the tiles before this one
+  for (long long base = 0; base < N; base += PREP_THREADS) {
+    const long long i = base + tid;
+    const bool v = i < N && target_valid(t[i], ii, V);
+    const unsigned bal = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) wsum[w] = __popc(bal);
+    __syncthreads();
+    if (w == 0) {   // exclusive scan of the warp counts
+      const int x = wsum[lane];
+      int incl = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      wsum[lane] = incl - x;
+      if (lane == 31) red[0] = incl;   // valid rows in this tile
+    }
+    __syncthreads();
+    const long long before = done + wsum[w] + __popc(bal & lt);   // valid rows before row i
+    if (i < N) idx[v ? before : total + (i - before)] = static_cast<int>(i);
+    done += red[0];
+    __syncthreads();
   }
   if (tid == 0) {
     hdr[HDR_STATUS] = bad ? STATUS_BADTARGET : 0;
