@@ -96,7 +96,10 @@ typedef struct flce_plan_info {
 } flce_plan_info;
 
 /*
- * Workspace sizes.
+ * Workspace sizes.  The workspace holds one chunk of tokens at a time: the
+ * chunked processing of the "efficient-llm-anatomy" README ("Fused
+ * cross-entropy computes backward during forward", and the memory the
+ * "Per-component memory savings" table measures for the cross-entropy row).
  * flce_workspace_bytes: the default plan, sized so that the extra device
  *   memory stays below 5% of the N*V*2 bytes that bf16 logits would take
  *   (never below one 128-row chunk).
@@ -143,7 +146,10 @@ flce_status flce_fwd_bwd(const void* hidden, const void* weight,
 
 /*
  * Forward only: loss (and optionally row_loss) without gradients, 2*N*H*V
- * flops instead of 6*N*H*V.  Same argument rules as flce_fwd_bwd.
+ * flops instead of 6*N*H*V: the masked mean of the per-token negative
+ * log-likelihoods ("Alisa's book of LLMs", "cross-entropy loss" and
+ * "implementing the loss"), each from a max-shifted log-sum-exp ("Numerical
+ * stability and other tricks").  Same argument rules as flce_fwd_bwd.
  */
 flce_status flce_loss(const void* hidden, const void* weight,
                       const int32_t* targets, int64_t N, int64_t H, int64_t V,
@@ -238,6 +244,7 @@ flce_status flce_scale_grads(void* grad_hidden, float* grad_weight, int64_t N,
                              void* stream);
 
 /*
+ * Error reporting of this library (the pages specify none).
  * Synchronises `stream`, then reads the device status word of the last call
  * that used `workspace`: FLCE_OK, FLCE_EBADTARGET or FLCE_ETIMEOUT (or
  * FLCE_ECUDA if the stream reports an error).
@@ -322,10 +329,11 @@ flce_status flce_profile_begin(void);
 flce_status flce_profile_end(double* gemm_ms /* [3] */, int64_t* gemm_launches /* [3] */,
                              int64_t* kernel_launches);
 
-/* Static English description of a status code. */
+/* Static English description of a status code (error reporting of this
+ * library; the pages specify none). */
 const char* flce_status_string(flce_status s);
 
-/* Library version, e.g. "0.1.0". */
+/* Library version, e.g. "0.1.0" (no counterpart in the pages). */
 const char* flce_version(void);
 
 #ifdef __cplusplus

@@ -206,17 +206,18 @@ def fwd_bwd(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, i
 def rmsnorm_fwd_bwd(hidden: torch.Tensor, gain: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                     eps: float = 1e-6, ignore_index: int = -100, reduction: str = "mean", *,
                     workspace: Optional[torch.Tensor] = None, row_loss: bool = False, out: Optional[dict] = None,
-                    stream=None) -> dict:
+                    stream=None, grad_weight_dtype=torch.float32) -> dict:
     """Final RMSNorm (x = h / rms(h) * gain) fused in front of the LM head loss.
 
     grad_hidden is the gradient with respect to the pre-norm hidden states;
-    grad_gain (fp32 [H]) and grad_weight (fp32 [V,H]) as the parameters'."""
+    grad_gain (fp32 [H]) and grad_weight ([V,H], fp32 or bf16) as the parameters'."""
     N, H, V = _check_inputs(hidden, weight, targets)
     if gain.dtype != torch.bfloat16 or gain.shape != (H,) or not gain.is_cuda or not gain.is_contiguous():
         raise ValueError("gain must be a contiguous bf16 CUDA tensor of shape [H]")
     dev = hidden.device
+    flags = _flags(reduction, grad_weight_dtype)
     if workspace is None:
-        nb = library().flce_rmsnorm_workspace_bytes(N, H, V, REDUCE[reduction])
+        nb = library().flce_rmsnorm_workspace_bytes(N, H, V, flags)
         if nb == 0:
             raise FlceError(FLCE_EINVAL, "workspace size")
         workspace = new_workspace(nb, dev)
@@ -226,10 +227,12 @@ def rmsnorm_fwd_bwd(hidden: torch.Tensor, gain: torch.Tensor, weight: torch.Tens
         o["n_valid"] = torch.empty(1, dtype=torch.int32, device=dev)
         o["grad_hidden"] = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
         o["grad_gain"] = torch.empty(H, dtype=torch.float32, device=dev)
-        o["grad_weight"] = torch.empty((V, H), dtype=torch.float32, device=dev)
+        o["grad_weight"] = torch.empty((V, H), dtype=grad_weight_dtype, device=dev)
         o["row_loss"] = torch.empty(N, dtype=torch.float32, device=dev) if row_loss else None
+    if o["grad_weight"].dtype != grad_weight_dtype:
+        raise TypeError("out['grad_weight'] does not have grad_weight_dtype")
     s = library().flce_rmsnorm_fwd_bwd(_ptr(hidden), _ptr(gain), float(eps), _ptr(weight), _ptr(targets), N, H, V,
-                                       int(ignore_index), REDUCE[reduction], _ptr(o["loss"]), _ptr(o["n_valid"]),
+                                       int(ignore_index), flags, _ptr(o["loss"]), _ptr(o["n_valid"]),
                                        _ptr(o.get("row_loss")), _ptr(o["grad_hidden"]), _ptr(o["grad_gain"]),
                                        _ptr(o["grad_weight"]), _ptr(workspace), workspace.numel(), _stream(stream))
     if s != FLCE_OK:

@@ -71,3 +71,21 @@ def test_rmsnorm_unit_gain_equals_plain_on_normalised_input(dev):
     b = flce.fwd_bwd(h, w, t)
     assert abs(float(a["loss"].item()) - float(b["loss"].item())) <= 2e-3 * abs(float(b["loss"].item()))
     assert frob_rel(a["grad_weight"].cpu().double().numpy(), b["grad_weight"].cpu().double().numpy()) <= 1e-2
+
+
+def test_rmsnorm_bf16_grad_weight(dev):
+    # FLCE_GW_BF16 on the fused-RMSNorm entry point: the same fp32 accumulation, rounded once
+    import torch
+    from linear_cross_entropy_ce_gb300 import flce
+    p = wl.random_problem(600, 128, 900, seed=5, ignore_frac=0.1, hidden_std=3.0)
+    g = _gain(128, 5)
+    h, w, t = to_device(p, dev)
+    gt = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).to(dev)
+    a = flce.rmsnorm_fwd_bwd(h, gt, w, t)
+    b = flce.rmsnorm_fwd_bwd(h, gt, w, t, grad_weight_dtype=torch.bfloat16)
+    assert flce.query_status(b["workspace"]) == flce.FLCE_OK
+    assert b["grad_weight"].dtype == torch.bfloat16
+    assert torch.equal(b["grad_weight"], a["grad_weight"].to(torch.bfloat16))
+    assert torch.equal(a["grad_hidden"], b["grad_hidden"]) and torch.equal(a["grad_gain"], b["grad_gain"])
+    ref = rmsnorm_flce_oracle(p["hidden"], g, p["weight"], p["targets"], 1e-6)
+    assert frob_rel(b["grad_weight"].double().cpu().numpy(), ref["grad_weight"]) <= GRAD_FROB_RTOL
