@@ -35,14 +35,23 @@ METRIC = "fused linear-CE fwd+bwd tokens/s and % of GB300 dense BF16 tensor peak
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# The sources that define and launch flce_gemm_kernel (the kernel whose DRAM
+# traffic the roofline reports): the kernel, its PTX helpers and shared
+# declarations, and the host code that plans and launches it.
+GEMM_SOURCES = ("flce_gemm.cu", "flce_ptx.cuh", "flce_internal.h", "flce_api.cu")
+
+
 def kernel_sources_sha1() -> str:
-    """Hash of the CUDA sources with comments and blank space removed, so that
-    DRAM counters taken on one build stay attached to it across comment edits."""
-    import glob
+    """Hash of the GEMM kernel's sources with comments and blank space removed,
+    so that DRAM counters taken on one build stay attached to it across
+    comment edits and changes to the other kernels."""
     import hashlib
     import re
     h = hashlib.sha1()
-    for f in sorted(glob.glob(os.path.join(ROOT, "linear_cross_entropy_ce_gb300", "csrc", "*"))):
+    for name in GEMM_SOURCES:
+        f = os.path.join(ROOT, "linear_cross_entropy_ce_gb300", "csrc", name)
+        if not os.path.exists(f):
+            continue
         with open(f, "r", encoding="utf-8") as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)

@@ -4,7 +4,8 @@
   line with the keys every bench line carries, plus its own `impl`,
   `cpu_baseline` and a zero-copy `e2e`.
 * The source hash that attaches the committed DRAM counters to a build
-  ignores comments and blank space but not code.
+  ignores comments and blank space but not code, and covers the GEMM
+  kernel's sources only.
 """
 import json
 import os
@@ -41,14 +42,17 @@ def test_source_hash_ignores_comments_only(tmp_path, monkeypatch):
     import bench
     src = tmp_path / "linear_cross_entropy_ce_gb300" / "csrc"
     src.mkdir(parents=True)
-    f = src / "k.cu"
+    f = src / "flce_gemm.cu"
     f.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  // one\n}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.kernel_sources_sha1()
     f.write_text("/* a new\n   comment */\n__global__   void k(int* p) {   p[0] = 1; }\n")
     assert bench.kernel_sources_sha1() == h0
     f.write_text("__global__ void k(int* p) { p[0] = 2; }\n")
-    assert bench.kernel_sources_sha1() != h0
+    h1 = bench.kernel_sources_sha1()
+    assert h1 != h0
+    (src / "flce_aux.cu").write_text("__global__ void other() {}\n")   # another kernel's source
+    assert bench.kernel_sources_sha1() == h1
 
 
 def test_committed_traffic_matches_committed_kernel():
