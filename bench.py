@@ -228,6 +228,7 @@ def run_reference(args):
 def run_variant(args) -> int:
     """Time one widened form of the path at the chosen workload:
 
+    loss            the forward-only loss (flce_loss: 2*n_valid*H*V flops)
     rmsnorm         the final RMSNorm fused in front (flce_rmsnorm_fwd_bwd)
     autograd        LinearCrossEntropy forward + backward with grad_output 2.5
                     (the library call plus the flce_scale_grads pass)
@@ -253,7 +254,16 @@ def run_variant(args) -> int:
     flops = 6.0 * nv * H * V
     cfg = {"workload": w.name, "N": N, "H": H, "V": V, "n_valid": nv}
 
-    if args.variant == "rmsnorm":
+    if args.variant == "loss":
+        ws = flce.new_workspace(flce.workspace_bytes(N, H, V, forward_only=True), dev)
+        out = {}
+
+        def step():
+            flce.loss(h, W, t, workspace=ws, out=out)
+        flops = 2.0 * nv * H * V
+        cfg["workspace_bytes"] = ws.numel()
+        cfg["flops_note"] = "2*n_valid*H*V (logits only)"
+    elif args.variant == "rmsnorm":
         gain = (1.0 + 0.1 * torch.randn(H, generator=torch.Generator().manual_seed(5))).to(torch.bfloat16).to(dev)
         ws = flce.new_workspace(flce.library().flce_rmsnorm_workspace_bytes(N, H, V, 0), dev)
         out = {}
@@ -328,7 +338,7 @@ def main():
     ap.add_argument("--chunk-rows", type=int, default=None, help="override the default 5%% plan")
     ap.add_argument("--workspace-bytes", type=int, default=None,
                     help="workspace size to plan for (small profiling cases that keep a full-size plan)")
-    ap.add_argument("--variant", default=None, choices=["rmsnorm", "autograd", "vocab_parallel"],
+    ap.add_argument("--variant", default=None, choices=["loss", "rmsnorm", "autograd", "vocab_parallel"],
                     help="time a widened form of the path instead (one GPU; not the contract line)")
     ap.add_argument("--shards", type=int, default=2, help="vocabulary shards for --variant vocab_parallel")
     args = ap.parse_args()
