@@ -354,3 +354,30 @@ def test_full_vocab_reduced_tokens(dev, name, N):
     # full H and V of the big workloads, fewer tokens so the oracle runs whole;
     # 128-row chunks exercise the fp32 grad_weight accumulation at full V
     check_full(wl.make_inputs(wl.WORKLOADS[name].with_shape(N=N)), dev, chunk_rows=128, case=f"{name}_N{N}")
+
+
+def test_concurrent_calls_on_two_streams(dev):
+    # Calls are reentrant: two problems enqueued on two streams at once, each
+    # with its own workspace and outputs, give bitwise the results of the same
+    # calls made one after the other (the tile counters and split flags live
+    # in each call's workspace; no kernel waits on another launch).
+    flce = _flce()
+    import torch
+    pa = wl.random_problem(1000, 256, 3000, seed=18, ignore_frac=0.1)
+    pb = wl.random_problem(700, 128, 5000, seed=19, ignore_frac=0.2)
+    ha, wa, ta = to_device(pa, dev)
+    hb, wb, tb = to_device(pb, dev)
+    ref_a = flce.fwd_bwd(ha, wa, ta, chunk_rows=256, row_loss=True)
+    ref_b = flce.fwd_bwd(hb, wb, tb, chunk_rows=128, row_loss=True)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            a = flce.fwd_bwd(ha, wa, ta, chunk_rows=256, row_loss=True, stream=s1)
+        with torch.cuda.stream(s2):
+            b = flce.fwd_bwd(hb, wb, tb, chunk_rows=128, row_loss=True, stream=s2)
+        torch.cuda.synchronize()
+        assert flce.query_status(a["workspace"]) == flce.FLCE_OK and flce.query_status(b["workspace"]) == flce.FLCE_OK
+        for k in ("loss", "n_valid", "row_loss", "grad_hidden", "grad_weight"):
+            assert torch.equal(a[k], ref_a[k]), k
+            assert torch.equal(b[k], ref_b[k]), k
