@@ -100,6 +100,8 @@ def test_tiny_workload(dev):
     (257, 8, 5000, 0.3, 128, 5),       # H = 8: one K block, mostly padding
     (256, 1024, 2000, 0.05, None, 6),  # 16 K blocks, one chunk
     (640, 256, 3001, 0.5, 256, 7),     # half the tokens ignored, odd V
+    (64, 8192, 300, 0.0, None, 20),    # wide hidden size: 128 K blocks, 32 grad_hidden column tiles
+    (20000, 64, 50, 0.3, None, 21),    # many tokens, a tiny vocabulary: 20 compaction tiles, V inside one tile
 ])
 def test_ragged_shapes(dev, N, H, V, ign, chunk, seed):
     check_full(wl.random_problem(N, H, V, seed=seed, ignore_frac=ign), dev, chunk_rows=chunk)
