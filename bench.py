@@ -527,6 +527,12 @@ def main():
             "flops_per_launch": flops_alg / max(1, gemm_n / args.steps),
             "avg_launch_ms": gemm_ms / max(1, gemm_n),
             "per_mode_ms_per_step": {k: v / args.steps for k, v in prof["gemm_ms"].items()}}
+    if traffic is not None:
+        # DRAM bytes the GEMM launches of one step move (ncu counters x launches) and their rate
+        per_step = traffic * gemm_n / args.steps
+        roof["dram_bytes_per_step"] = per_step
+        roof["dram_gbs_during_gemm"] = per_step / (gemm_ms / args.steps / 1000.0) / 1e9
+        roof["dram_frac_of_peak"] = roof["dram_gbs_during_gemm"] / float(pk["hbm_gbs"])
     line = {
         "metric": METRIC, "value": world * N / (ms / 1000.0), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
