@@ -12,7 +12,7 @@
 //     dX units   dX = dz W            A = dz [C,V] K-major,  B = W [V,H] MN-major
 //                epilogue: bf16 rows of grad_hidden, scattered to token rows;
 //                with the vocabulary split in S parts, the parts are summed in
-//                fp32 in split order (TMA store, then reduce-adds, each part
+//                fp32 in split order (a store, then L2 reduce-adds, each part
 //                waiting for the previous one), and the last part converts.
 //     dW units   dW (+)= dz^T Xc      A = dz^T (MN-major view of dz), B = Xc MN-major
 //                epilogue: fp32 tile staged in shared memory and written by a
@@ -31,11 +31,12 @@
 // in the logits launch, whose epilogue needs no staging buffers; in CTA 0 it
 // also claims tiles from a global counter and hands them to both CTAs),
 // warp 1 allocates TMEM and, in CTA 0, one lane issues the MMAs for the pair,
-// warps 2-9 (two warpgroups, one per 128-column half) drain two TMEM
-// accumulators (double buffered, 2 x 256 columns) so an epilogue overlaps the
-// next tile's main loop.  Every wait is
-// bounded: on time-out a CTA raises an abort flag, lets copies in flight
-// land, frees TMEM and returns, and the workspace status word records
+// and warps 2-17 are the epilogue: two sets of two warpgroups, set e draining
+// TMEM accumulator e (double buffered, 2 x 256 columns), one 128-column half
+// per warpgroup, so the epilogues of two consecutive tiles run at once and
+// both overlap the next tile's main loop.  Every wait is bounded: on time-out
+// a CTA raises an abort flag, lets copies in flight land, waits for its MMAs,
+// frees TMEM and returns, and the workspace status word records
 // STATUS_TIMEOUT.
 #include "flce_internal.h"
 #include "flce_ptx.cuh"
