@@ -102,6 +102,8 @@ def test_tiny_workload(dev):
     (640, 256, 3001, 0.5, 256, 7),     # half the tokens ignored, odd V
     (64, 8192, 300, 0.0, None, 20),    # wide hidden size: 128 K blocks, 32 grad_hidden column tiles
     (20000, 64, 50, 0.3, None, 21),    # many tokens, a tiny vocabulary: 20 compaction tiles, V inside one tile
+    (2600, 136, 20000, 0.1, 1536, 22), # two chunks of 6 and 5 row blocks x 79 vocabulary tiles, ragged H and V
+    (1200, 512, 16000, 0.05, 768, 23), # the full-model H and V in 768-row chunks, a 432-row last chunk
 ])
 def test_ragged_shapes(dev, N, H, V, ign, chunk, seed):
     check_full(wl.random_problem(N, H, V, seed=seed, ignore_frac=ign), dev, chunk_rows=chunk)
