@@ -389,9 +389,7 @@ flce_status run(const Job& j) {
     ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, j.weight, H, V, hb, 64, BK) &&
          make_map(&bm.a1, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&bm.b1, xc, H, p.C, hb, 64, BK) &&
          make_map(&bm.out, gwacc, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B) &&
-         make_map(&bm.pf, gwacc, H, V, static_cast<unsigned long long>(H) * 4, BN, BM,
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE);
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return FLCE_ECUDA;
 
   const int reduce_sum = (j.flags & FLCE_REDUCE_SUM) ? 1 : 0;
@@ -418,10 +416,12 @@ flce_status run(const Job& j) {
   g.splits = p.splits;
   g.kb_per_split = p.kb_per_split;
   g.interleave = 1;
-  // grad_weight tiles of <= 8 K blocks are bound by their epilogue and the TMA
-  // unit: prefetch their grad_weight blocks from the epilogue threads instead
-  // (large-vocabulary workload, C = 384: backward -3.6%; at C = 768 the TMA
-  // prefetch, issued a whole main loop ahead, is 1.5% better)
+  // grad_weight tiles of <= 8 K blocks are bound by their epilogue: the
+  // epilogue threads pull the next grad_weight block into L2 with plain
+  // prefetches (large-vocabulary workload, C = 384: the backward is 4% slower
+  // without them).  Longer tiles prefetch nothing: a TMA prefetch of the block
+  // at the tile start queued in front of the tile's loads and cost 0.6-2%
+  // (Llama-3-8B head, full-model shape).
   g.pf_threads = p.C <= 512 ? 1 : 0;
   g.dxacc = dxacc;
 

@@ -78,7 +78,7 @@ struct GemmArgs {
 // b1 = Xc (MN-major), out = grad_weight (fp32, store / reduce-add of 16 x 128
 // slices), pf = grad_weight again with a 256 x 128 box for L2 prefetches.
 struct GemmMaps {
-  CUtensorMap a0, b0, a1, b1, out, pf;
+  CUtensorMap a0, b0, a1, b1, out;
 };
 
 int gemm_smem_bytes();
