@@ -523,6 +523,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < SCHED_SLOTS; ++i) {
       ptx::mbar_init(&ctl->sfull[i], 1);
       ptx::mbar_init(&ctl->sempty[i], SCHED_READERS);
+      // CTA 1's slots are filled by CTA 0's st.async: its producer arms each
+      // phase with the 4 bytes to expect (this one, then after each read)
+      if (rank == 1) ptx::mbar_arrive_expect_tx(&ctl->sfull[i], 4);
     }
     ptx::mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
@@ -569,13 +572,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         u = next < s.units ? next : -1;
         next = -1;
         ctl->sunit[sslot] = u;
-        ptx::st_remote_u32(ptx::map_to_rank(&ctl->sunit[sslot], 1), static_cast<uint32_t>(u));
         ptx::mbar_arrive(&ctl->sfull[sslot]);
-        ptx::mbar_arrive_remote(ptx::map_to_rank(&ctl->sfull[sslot], 1));
+        // the peer's copy goes by st.async, which completes the transaction
+        // armed on the peer's slot barrier; a release arrive here would wait
+        // for this thread's TMA loads in flight (~1 us per grad_weight tile)
+        ptx::st_async_u32(ptx::map_to_rank(&ctl->sunit[sslot], 1), static_cast<uint32_t>(u),
+                          ptx::map_to_rank(&ctl->sfull[sslot], 1));
       } else {
         if (!wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_PRODUCER)) { ok = false; break; }
-        u = ctl->sunit[sslot];
-        ptx::mbar_arrive_remote(ptx::map_to_rank(&ctl->sempty[sslot], 0));
+        u = ptx::ld_acquire_shared(&ctl->sunit[sslot]);
+        ptx::mbar_arrive_expect_tx(&ctl->sfull[sslot], 4);   // arm the slot's next phase
+        // hand the slot back; relaxed (the acquire load above orders it after
+        // the read), since a release would wait for this thread's TMA loads
+        ptx::mbar_arrive_remote_relaxed(ptx::map_to_rank(&ctl->sempty[sslot], 0));
       }
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
@@ -680,9 +689,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       // every wait is followed by a vote so that all threads of the set leave together
       bool ok = wait_phase(&ctl->sfull[sslot], sphase, ctl, to, true, hdr, W_SCHED_FULL_EPI, sslot << 24);
       if (!ptx::named_bar_and(sbar, SET_THREADS, ok)) break;
-      const int u = ctl->sunit[sslot];
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_remote(sempty0 + sslot * 8u);
+      // lane 0 reads the slot and hands it back; relaxed (its acquire load
+      // orders the arrive after the read), since a release would wait for
+      // the warp's row stores in flight
+      int u = 0;
+      if (lane == 0) {
+        u = ptx::ld_acquire_shared(&ctl->sunit[sslot]);
+        ptx::mbar_arrive_remote_relaxed(sempty0 + sslot * 8u);
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
       if (++sslot == SCHED_SLOTS) { sslot = 0; sphase ^= 1u; }
       if (u < 0) break;
       if ((seq++ & 1u) != static_cast<uint32_t>(set)) continue;   // the other set's tile

@@ -78,9 +78,23 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Relaxed form: no ordering of this thread's earlier memory writes (a release
-// arrive waits until its outstanding global stores are visible).
+// arrive waits until its outstanding memory operations are performed).
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Store 4 bytes into a CTA of the cluster and count them as a transaction on
+// an mbarrier there (whose phase must expect them), without a release fence.
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v, uint32_t bar_cluster_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(cluster_addr), "r"(v),
+               "r"(bar_cluster_addr)
+               : "memory");
+}
+// Shared-memory load with acquire semantics: later memory operations of this
+// thread (for instance a relaxed mbarrier arrive) are ordered after it.
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
 }
 __device__ __forceinline__ void st_remote_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
