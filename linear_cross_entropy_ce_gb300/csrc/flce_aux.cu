@@ -67,10 +67,12 @@ constexpr int PREP_WARPS = PREP_THREADS / 32;
 
 __device__ __forceinline__ bool target_valid(int x, int ii, int V) { return x != ii && x >= 0 && x < V; }
 
+constexpr int PREP_PER = 8;   // consecutive rows per thread in pass 2
+
 // One block: pass 1 counts the valid targets (coalesced reads); pass 2 walks
-// the targets in tiles of 1024 and places every row with a warp ballot and a
-// scan of the 32 warp counts: valid rows in order first, then the others in
-// order.
+// the targets in tiles of 8192 (8 consecutive rows per thread) and places
+// every row by a scan of the thread counts within each warp and of the 32
+// warp counts: valid rows in order first, then the others in order.
 __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restrict__ t, long long N, int V,
                                                              int ii, int* hdr, int* __restrict__ idx,
                                                              int* n_valid_out, int* counters,
@@ -89,28 +91,44 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const int* __restric
   }
   const int total = block_reduce(c, AddOp(), 0, red);
   if (mybad) bad = 1;
-  const unsigned lt = (1u << lane) - 1u;
   long long done = 0;   // valid rows in the tiles before this one
-  for (long long base = 0; base < N; base += PREP_THREADS) {
-    const long long i = base + tid;
-    const bool v = i < N && target_valid(t[i], ii, V);
-    const unsigned bal = __ballot_sync(0xffffffffu, v);
-    if (lane == 0) wsum[w] = __popc(bal);
+  for (long long base = 0; base < N; base += static_cast<long long>(PREP_THREADS) * PREP_PER) {
+    const long long i0 = base + static_cast<long long>(tid) * PREP_PER;
+    unsigned m = 0;   // bit j: row i0 + j is valid
+#pragma unroll
+    for (int j = 0; j < PREP_PER; ++j)
+      if (i0 + j < N && target_valid(t[i0 + j], ii, V)) m |= 1u << j;
+    const int c = __popc(m);
+    int incl = c;   // inclusive scan of the thread counts in the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[w] = incl;
     __syncthreads();
     if (w == 0) {   // exclusive scan of the warp counts
       const int x = wsum[lane];
-      int incl = x;
+      int winc = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        const int y = __shfl_up_sync(0xffffffffu, winc, o);
+        if (lane >= o) winc += y;
       }
-      wsum[lane] = incl - x;
-      if (lane == 31) red[0] = incl;   // valid rows in this tile
+      wsum[lane] = winc - x;
+      if (lane == 31) red[0] = winc;   // valid rows in this tile
     }
     __syncthreads();
-    const long long before = done + wsum[w] + __popc(bal & lt);   // valid rows before row i
-    if (i < N) idx[v ? before : total + (i - before)] = static_cast<int>(i);
+    long long before = done + wsum[w] + (incl - c);   // valid rows before row i0
+#pragma unroll
+    for (int j = 0; j < PREP_PER; ++j) {
+      const long long i = i0 + j;
+      if (i < N) {
+        const bool v = (m >> j) & 1u;
+        idx[v ? before : total + (i - before)] = static_cast<int>(i);
+        before += v ? 1 : 0;
+      }
+    }
     done += red[0];
     __syncthreads();
   }
@@ -257,6 +275,12 @@ __global__ void __launch_bounds__(FIN_THREADS)
                     int reduce_sum, float* loss, int* n_valid_out, float* row_loss) {
   __shared__ double red[FIN_THREADS / 32];
   const long long nv = hdr[HDR_NVALID];
+  if (row_loss)   // every block: the per-token losses back in token order
+    for (long long i = static_cast<long long>(blockIdx.x) * FIN_THREADS + threadIdx.x; i < N;
+         i += static_cast<long long>(gridDim.x) * FIN_THREADS)
+      row_loss[idx[i]] = i < nv ? rl[i] : 0.f;
+  if (blockIdx.x != 0) return;
+  // block 0: the loss, summed in fp64 in a fixed order
   double s = 0.0;
   for (long long i = threadIdx.x; i < nv; i += FIN_THREADS) s += rl[i];
   s = block_reduce(s, AddOp(), 0.0, red);
@@ -269,8 +293,6 @@ __global__ void __launch_bounds__(FIN_THREADS)
                    : (nv == 0 ? 0.f : static_cast<float>(reduce_sum ? s : s / static_cast<double>(nv)));
     if (n_valid_out) *n_valid_out = static_cast<int>(nv);
   }
-  if (row_loss)
-    for (long long i = threadIdx.x; i < N; i += FIN_THREADS) row_loss[idx[i]] = i < nv ? rl[i] : 0.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -574,7 +596,8 @@ cudaError_t launch_lse_dz(const int* hdr, long long c0, int C, int V, long long 
 
 cudaError_t launch_finalize(const int* hdr, const int* idx, const float* rl, long long N, int reduce_sum,
                             float* loss, int* n_valid_out, float* row_loss, cudaStream_t s) {
-  finalize_kernel<<<1, FIN_THREADS, 0, s>>>(hdr, idx, rl, N, reduce_sum, loss, n_valid_out, row_loss);
+  const int blocks = row_loss ? static_cast<int>(std::min<long long>((N + 4 * FIN_THREADS - 1) / (4 * FIN_THREADS), 148)) : 1;
+  finalize_kernel<<<blocks, FIN_THREADS, 0, s>>>(hdr, idx, rl, N, reduce_sum, loss, n_valid_out, row_loss);
   return cudaGetLastError();
 }
 
