@@ -388,8 +388,8 @@ flce_status run(const Job& j) {
   if (!fwd_only)
     ok = ok && make_map(&bm.a0, z, V, p.C, p.ldz * 2, BK, BM) && make_map(&bm.b0, j.weight, H, V, hb, 64, BK) &&
          make_map(&bm.a1, z, V, p.C, p.ldz * 2, 64, BK) && make_map(&bm.b1, xc, H, p.C, hb, 64, BK) &&
-         make_map(&bm.out, gwacc, H, V, static_cast<unsigned long long>(H) * 4, 16, BM,
-                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_64B);
+         make_map(&bm.out, gwacc, H, V, static_cast<unsigned long long>(H) * 4, 32, 64,
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return FLCE_ECUDA;
 
   const int reduce_sum = (j.flags & FLCE_REDUCE_SUM) ? 1 : 0;

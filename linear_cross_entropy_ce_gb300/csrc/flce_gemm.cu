@@ -49,8 +49,14 @@ constexpr int STAGES_LOGITS = 7;            // the logits epilogue stages nothin
 constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SLICE_COLS = 16;              // fp32 columns per staged output slice (64 B rows)
-constexpr int STG_BYTES = BM * SLICE_COLS * 4;   // one 128 x 16 fp32 slice: 8 KB
+constexpr int SLICE_COLS = 16;              // fp32 columns per staged slice of a split grad_hidden part (64 B rows)
+// grad_weight leaves through TMA boxes of 64 rows x 32 fp32 columns (128-byte
+// rows, 8 KB, one warpgroup's staging buffer); 128-byte rows halve the row
+// requests of 64-byte ones
+constexpr int OUT_COLS = 32;
+constexpr int OUT_ROWS = 64;
+constexpr int STG_BYTES = BM * SLICE_COLS * 4;   // a warpgroup's staging buffer: 8 KB
+static_assert(OUT_ROWS * OUT_COLS * 4 == STG_BYTES, "one grad_weight box fills a staging buffer");
 // Two epilogue sets, one per TMEM accumulator, so that the epilogues of two
 // consecutive tiles run at once (tiles with few K blocks are bound by their
 // epilogue); each set has two warpgroups, one per 128-column half.
@@ -361,41 +367,46 @@ __device__ __forceinline__ void epi_dx_direct(const GemmArgs& a, const Shape& s,
   }
 }
 
-// The warpgroup's 128 x 128 fp32 accumulator block -> 16-column slices ->
-// shared memory (64-byte rows, 64-byte swizzle: chunk g of row r sits at
-// g ^ ((r >> 1) & 3), conflict-free) -> TMA store (reduce == false) or TMA
-// reduce-add into `map` at (h, row0).  One staging buffer per warpgroup (the
-// four warpgroups keep the TMA unit busy between them); `leader` (one thread
-// of the warpgroup) owns the bulk groups.  The next slice's TMEM load is
-// issued before the wait for the buffer.
+// The warpgroup's 128 x 128 fp32 accumulator block -> 32-column slices, each
+// in two boxes of 64 rows -> shared memory (128-byte rows, 128-byte swizzle:
+// chunk g of row rr sits at g ^ (rr & 7)) -> TMA store (reduce == false) or
+// TMA reduce-add into `map` at (h, row0 + 64 b).  One 8 KB staging buffer per
+// warpgroup (the four warpgroups keep the TMA unit busy between them), which
+// the two row halves take in turn; `leader` (one thread of the warpgroup)
+// owns the bulk groups.
 __device__ __forceinline__ void block_to_global(const CUtensorMap* map, int ncols_total, int h0, int row0,
                                                 bool reduce, uint32_t tbase, int r, bool leader, uint32_t bar,
                                                 uint8_t* buf) {
   const int left = ncols_total - h0;
-  const int nsl = left <= 0 ? 0 : min(GROUP_COLS / SLICE_COLS, (left + SLICE_COLS - 1) / SLICE_COLS);
+  const int nsl = left <= 0 ? 0 : min(GROUP_COLS / OUT_COLS, (left + OUT_COLS - 1) / OUT_COLS);
   if (nsl == 0) return;   // uniform over the warpgroup
-  float v[SLICE_COLS];
-  ptx::tmem_ld16(tbase, v);
+  const int half = r / OUT_ROWS, rr = r % OUT_ROWS;   // the box (64 rows) this thread's row goes in
+  uint8_t* row = buf + rr * (OUT_COLS * 4);
 #pragma unroll 1
   for (int j = 0; j < nsl; ++j) {
-    const int h = h0 + j * SLICE_COLS;
-    if (leader) ptx::bulk_wait_read_0();          // the previous slice's store has read the buffer
-    ptx::named_bar_sync(bar, GROUP_THREADS);
-    uint8_t* row = buf + r * (SLICE_COLS * 4);
+    float v[OUT_COLS];
+    ptx::tmem_ld32(tbase + j * OUT_COLS, v);
+    const int h = h0 + j * OUT_COLS;
+#pragma unroll 1
+    for (int b = 0; b < BM / OUT_ROWS; ++b) {
+      if (leader) ptx::bulk_wait_read_0();          // the previous box's store has read the buffer
+      ptx::named_bar_sync(bar, GROUP_THREADS);
+      if (half == b) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
-      *reinterpret_cast<float4*>(row + ((g ^ ((r >> 1) & 3)) << 4)) =
-          make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-    ptx::fence_proxy_async_smem();
-    ptx::named_bar_sync(bar, GROUP_THREADS);
-    if (leader) {
-      if (reduce)
-        ptx::tma_reduce_add_2d(map, buf, h, row0);
-      else
-        ptx::tma_store_2d(map, buf, h, row0);
-      ptx::bulk_commit();
+        for (int g = 0; g < OUT_COLS / 4; ++g)      // 128-byte swizzle: 16-byte chunk g of row rr
+          *reinterpret_cast<float4*>(row + ((g ^ (rr & 7)) << 4)) =
+              make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        ptx::fence_proxy_async_smem();
+      }
+      ptx::named_bar_sync(bar, GROUP_THREADS);
+      if (leader) {
+        if (reduce)
+          ptx::tma_reduce_add_2d(map, buf, h, row0 + b * OUT_ROWS);
+        else
+          ptx::tma_store_2d(map, buf, h, row0 + b * OUT_ROWS);
+        ptx::bulk_commit();
+      }
     }
-    if (j + 1 < nsl) ptx::tmem_ld16(tbase + (j + 1) * SLICE_COLS, v);
   }
 }
 

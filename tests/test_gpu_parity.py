@@ -155,6 +155,30 @@ def test_deterministic(dev):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("N,H,V,chunk", [
+    (2048, 512, 20000, None),   # default 5% plan: 128-row chunks, the grad_hidden GEMM split over the vocabulary
+    (1536, 1024, 12000, 768),   # two 768-row chunks, unsplit grad_hidden GEMM, many short grad_weight tiles
+])
+def test_repeated_calls_bitwise(dev, N, H, V, chunk):
+    # The tile scheduler is dynamic (CTA pairs claim tiles from a counter and
+    # hand them to the peer CTA), so every call runs a different interleaving;
+    # the results must not change by a bit, and every call must end with an
+    # OK status.
+    flce = _flce()
+    import torch
+    p = wl.random_problem(N, H, V, seed=31, ignore_frac=0.1)
+    h, w, t = to_device(p, dev)
+    ref = flce.fwd_bwd(h, w, t, chunk_rows=chunk)
+    assert flce.query_status(ref["workspace"]) == flce.FLCE_OK
+    ref = {k: v.clone() for k, v in ref.items() if k != "workspace" and isinstance(v, torch.Tensor)}
+    out = None
+    for _ in range(20):
+        out = flce.fwd_bwd(h, w, t, chunk_rows=chunk, out=out)
+        assert flce.query_status(out["workspace"]) == flce.FLCE_OK
+        for k in ("loss", "n_valid", "grad_hidden", "grad_weight"):
+            assert torch.equal(out[k], ref[k]), k
+
+
 def test_ignored_rows_do_not_matter(dev):
     flce = _flce()
     import torch
