@@ -15,9 +15,10 @@
 //                fp32 in split order (a store, then L2 reduce-adds, each part
 //                waiting for the previous one), and the last part converts.
 //     dW units   dW (+)= dz^T Xc      A = dz^T (MN-major view of dz), B = Xc MN-major
-//                epilogue: fp32 tile staged in shared memory and written by a
-//                TMA store (first chunk) or a TMA reduce-add (later chunks),
-//                so the fp32 accumulation happens in L2 in fixed chunk order.
+//                epilogue: fp32 tile staged in shared memory, 64 x 32 boxes
+//                of 128-byte rows, and written by a TMA store (first chunk)
+//                or a TMA reduce-add (later chunks), so the fp32 accumulation
+//                happens in L2 in fixed chunk order.
 //                dX units are bound by the tensor cores, dW units (short, 12
 //                K blocks at C = 768) by the latency of their loads under the
 //                grad_weight read-modify-write: where the grad_hidden GEMM is
@@ -29,7 +30,10 @@
 // A and its 128 columns of B (32 KB per K block) and holds 128 accumulator
 // rows in its TMEM.  Per CTA: warp 0 issues TMA loads into a 6-stage ring (7
 // in the logits launch, whose epilogue needs no staging buffers; in CTA 0 it
-// also claims tiles from a global counter and hands them to both CTAs),
+// also claims tiles from a global counter and hands them to both CTAs, to
+// CTA 1 by st.async into a scheduler slot; slots and accumulators are handed
+// back with relaxed arrives, since a release arrive waits for the thread's
+// loads or stores in flight),
 // warp 1 allocates TMEM and, in CTA 0, one lane issues the MMAs for the pair,
 // and warps 2-17 are the epilogue: two sets of two warpgroups, set e draining
 // TMEM accumulator e (double buffered, 2 x 256 columns), one 128-column half
