@@ -127,11 +127,18 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
   p.o_xc = off;   off += al256(size_t(C) * H * 2);
   p.o_tc = off;   off += al256(size_t(C) * 4);
   p.o_zt = off;   off += al256(size_t(C) * 4);
-  p.o_part = off; off += al256(size_t(C) * p.nparts * 8);
-  if (!fwd_only) {
-    p.o_z = off; off += al256(size_t(C) * p.ldz * 2);
-    if (p.splits > 1) { p.o_dx = off; off += al256(size_t(C) * H * 4); }
+  if (!fwd_only) { p.o_z = off; off += al256(size_t(C) * p.ldz * 2); }
+  // The per-part (max, sum exp) of a chunk are read by lse_dz before the
+  // backward launch, and the fp32 sum of a split grad_hidden GEMM lives only
+  // inside that launch (the next chunk's logits rewrite the parts after it):
+  // the two share their bytes.
+  p.o_part = off;
+  size_t shared = al256(size_t(C) * p.nparts * 8);
+  if (!fwd_only && p.splits > 1) {
+    p.o_dx = off;
+    shared = std::max(shared, al256(size_t(C) * H * 4));
   }
+  off += shared;
   if (norm) {   // final RMSNorm: 1/rms per chunk row, d(gain) partial per chunk
     p.o_rinv = off; off += al256(size_t(C) * 4);
     p.o_dg = off;   off += al256(size_t(p.n_chunks) * H * 4);
@@ -142,8 +149,9 @@ Plan layout(long long N, long long H, long long V, long long C, int S, bool fwd_
 }
 
 // Vocabulary splits of the grad_hidden GEMM.  A dX tile (K = V) should take at
-// most half of a pair's average share of the backward launch, or it alone
-// sets the launch's length.  The parts of a tile are summed one after
+// most a pair's average share of the backward launch, or it alone sets the
+// launch's length (full-model shape: 2 splits 1.77 ms of backward per step,
+// 4 splits 2.28 ms, 1 split 1.90 ms).  The parts of a tile are summed one after
 // another, each waiting for the previous one to land (a few µs each), so the
 // chain of S parts costs S of those steps unless the dX units are spread
 // through the dW units (the kernel does that when the dW units outnumber what
@@ -157,7 +165,7 @@ int preferred_splits(long long C, long long H, long long V, int pairs) {
   const double unit = double(PAIR_M) * BN * double(V);
   const double work = dx_tiles * unit + double(cdiv(V, PAIR_M)) * double(cdiv(H, BN)) * PAIR_M * BN * double(C);
   const double per_pair = work / double(pairs);
-  const long long balance = static_cast<long long>(std::ceil(unit / (0.5 * per_pair)));
+  const long long balance = static_cast<long long>(std::ceil(unit / per_pair));
   const long long max_by_k = std::max<long long>(1, kbt / 8);   // >= 8 K blocks per split
   auto clamp = [&](long long S) {
     return std::max<long long>(1, std::min<long long>(std::min<long long>(S, MAX_SPLITS), max_by_k));

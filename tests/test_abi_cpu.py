@@ -66,7 +66,7 @@ def test_default_workspace_within_five_percent(lib, name):
 # has no room for the split accumulator inside 5% of its logits; the component
 # shape cannot spread its split units through the few grad_weight units, so
 # the split count balances unit length against the ordered chain of splits.
-PLANS = {"component": (128, 4), "full_model": (2944, 1), "llama3_8b_head": (768, 1), "large_vocab": (384, 16),
+PLANS = {"component": (128, 4), "full_model": (2944, 2), "llama3_8b_head": (768, 1), "large_vocab": (384, 16),
          "large_vocab_tail": (384, 16)}
 
 
